@@ -1,0 +1,221 @@
+/*
+ * pa.h - paged GQA decode / speculative-verify attention for one GB300 GPU.
+ *
+ * C ABI of libpa.  Every entry point takes plain pointers and sizes; no C++ or
+ * PyTorch type crosses this boundary.  Unless a comment says "host", a pointer
+ * is a DEVICE pointer on the current CUDA device.  The caller owns every
+ * buffer; the library allocates no device memory, keeps no per-call state
+ * (it caches only the SM count of each device it has launched on), never
+ * synchronises inside a decode call, and may be called from several host
+ * threads at once.  Both decode calls are stream-ordered and can be captured
+ * in a CUDA graph: every launch parameter is passed by value, so a graph never
+ * refers to host memory that a later call could overwrite ("SM70 attention and
+ * quantized projection coverage across TP sizes", section "Graph replay and
+ * long-prefill follow-up": symbol values as kernel arguments, no captured
+ * host stack addresses).
+ *
+ * Operation (both variants).  For request b < batch, verify query
+ * qi < q_len and query head h < num_q_heads, with G = num_q_heads /
+ * num_kv_heads, KV head g = h / G and L = ctx_lens[b]:
+ *
+ *     key j (0 <= j <= L - q_len + qi) lives in page block_table[b][j / page_size],
+ *     slot j % page_size;  s_j = (q . k_j) / sqrt(head_dim);
+ *     out[b][qi][h] = sum_j softmax(s)_j v_j.
+ *
+ * The q_len verify queries are the last q_len tokens of the context, so query
+ * qi sees one more key than query qi - 1 (causal speculative verify:
+ * "DFlash2 concurrent long-context attention", sections "Why the
+ * single-request optimization was missing from concurrent decode" and
+ * "Matched endpoint gate": q7/q8 verify steps over a paged E4M3 cache).  A row
+ * that sees no key (L = 0, a padded slot, or L < q_len - qi) is written as
+ * +0.0 in every element and Q for it is never read; a request with L = 0 never
+ * reads its block-table row ("padded requests and zero-length rows remain
+ * safe", same section).
+ *
+ * The G query heads x q_len queries that share one KV head are computed as one
+ * packed tile, so every KV byte is read once per KV head rather than once per
+ * query head ("perf(fa2): port decode GQA group-swap into d128 varlen
+ * launcher", vllm.cpp pull request #48, description: KV is read once per
+ * group).  Long contexts are cut into splits whose count depends only on that
+ * request's length; each split writes FP32 (m, l, O) partials into the
+ * request-major workspace and a log-sum-exp combine merges them in ascending
+ * split order ("DFlash2 concurrent long-context attention", same section:
+ * independent request-major workspace panels).  Results therefore do not
+ * depend on batch composition: a batched call writes, bit for bit, what one
+ * call per request writes ("Operator validation": batched results equal
+ * independent single-request execution bitwise).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+/* Return codes.  Every host-detectable problem is reported before any launch;
+ * nothing is written to out, lse or workspace in that case. */
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer (or params/caps struct) is NULL */
+  PA_ERR_SHAPE = -2,       /* batch, heads, q_len, page size, pool, lengths or strides out of range */
+  PA_ERR_UNSUPPORTED = -3, /* head_dim or GQA geometry this library does not implement */
+  PA_ERR_ALIGN = -4,       /* a pointer or stride is not a multiple of 8 bytes (16 for q/out/lse) */
+  PA_ERR_WORKSPACE = -5,   /* workspace NULL, not 256-byte aligned, or smaller than *_workspace_bytes() */
+  PA_ERR_CUDA = -6         /* a CUDA runtime call or a kernel launch failed */
+} pa_status;
+
+/* Bits of the 32-bit status word at the start of the workspace.  Kernels OR
+ * them in when a data-dependent check fails; the affected request's rows are
+ * then written as zeros instead of reading out of range.  The word is sticky:
+ * it keeps its bits across calls until pa_clear_status(). */
+#define PA_FLAG_BAD_PAGE 0x1u   /* a block-table entry for a visible key is outside [0, num_pages) */
+#define PA_FLAG_BAD_LENGTH 0x2u /* ctx_lens[b] < 0 or ctx_lens[b] > max_ctx_len */
+#define PA_FLAG_TIMEOUT 0x4u    /* an internal pipeline wait exceeded its bound; output of that call is invalid */
+
+/* Capabilities of the loaded library (host struct).  A caller compares these
+ * with what it is about to pass, so a stale binary is never handed shapes it
+ * cannot serve ("DFlash2 concurrent long-context attention", section "Why the
+ * single-request optimization was missing from concurrent decode": the loaded
+ * extension reports its batch capacity; "SM70 attention and quantized
+ * projection coverage across TP sizes", section "Compiled-library precision
+ * admission": the library reports its QK/PV accumulation bits, and section
+ * "Additional findings": positive 16-aligned page sizes are admitted and
+ * advertised by a capability query). */
+typedef struct pa_caps {
+  int32_t abi_version;   /* PA_ABI_VERSION */
+  int32_t max_batch;     /* largest batch (request slots) per call */
+  int32_t max_q_len;     /* largest verify window q_len */
+  int32_t max_group;     /* largest num_q_heads / num_kv_heads */
+  int32_t page_multiple; /* page_size must be a positive multiple of this */
+  int32_t max_ctx;       /* largest max_ctx_len */
+  int32_t accum_bits;    /* width of the QK and PV accumulators: 32 */
+  int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8: 256 */
+  int32_t bf16_head_dim; /* head_dim of pa_decode_bf16_d128: 128 */
+  int32_t reserved[7];
+} pa_caps;
+
+/* Geometry of one call (host struct, read during the call only). */
+typedef struct pa_params {
+  int32_t batch;             /* request slots B, 1 .. max_batch (padded slots have ctx_lens 0) */
+  int32_t num_kv_heads;      /* Hkv >= 1 */
+  int32_t num_q_heads;       /* Hq = G * Hkv, 1 <= G <= max_group */
+  int32_t head_dim;          /* D: 256 for pa_decode_fp8, 128 for pa_decode_bf16_d128 */
+  int32_t q_len;             /* verify queries per request, 1 .. max_q_len (bf16: 1 .. max_q_len too) */
+  int32_t page_size;         /* tokens per page, a positive multiple of page_multiple */
+  int32_t max_pages_per_req; /* block_table row length; >= ceil(max_ctx_len / page_size) */
+  int32_t num_pages;         /* pages in the pool; valid page ids are 0 .. num_pages-1 */
+  int32_t max_ctx_len;       /* host upper bound of every ctx_lens[b]; sizes grid and workspace */
+  int32_t reserved0;
+  /* byte strides of K and V: element (page p, slot t, kv head g, d) of K is at
+   * k_pages + p*k_page_stride + t*k_token_stride + g*k_head_stride + d*elem_bytes,
+   * V likewise.  Any layout is accepted (separate K/V tensors [pages, page_size,
+   * Hkv, D], or K and V interleaved per token and head) as long as every stride
+   * and both base pointers are multiples of 8 bytes; 16-byte multiples select
+   * 16-byte vector loads ("DFlash2 concurrent long-context attention",
+   * section "Operator validation": interleaved and eight-byte-only aligned KV
+   * strides). */
+  int64_t k_page_stride, k_token_stride, k_head_stride;
+  int64_t v_page_stride, v_token_stride, v_head_stride;
+} pa_params;
+
+/* Fills *out (host).  Returns PA_OK or PA_ERR_NULL. */
+int pa_get_capabilities(pa_caps* out);
+
+/* Static description of a status code (host string, never NULL). */
+const char* pa_status_string(int status);
+
+/* Host copy of the split planner the kernels run on the device: a request of
+ * ctx_len keys is cut into *num_splits consecutive splits of *chunk keys (the
+ * last one shorter).  Depends on ctx_len only, never on the batch.  ctx_len 0
+ * gives 0 splits.  Returns PA_ERR_NULL or PA_ERR_SHAPE (ctx_len < 0). */
+int pa_split_plan(int32_t ctx_len, int32_t* num_splits, int32_t* chunk);
+
+/* ---- FP16 Q x E4M3 K/V, head_dim 256 ---------------------------------------
+ *
+ * Workspace bytes a pa_decode_fp8 call with this geometry needs (0 when the
+ * geometry is invalid).  The workspace holds the status word and the
+ * request-major FP32 split partials; its content between calls is only the
+ * status word. */
+size_t pa_decode_fp8_workspace_bytes(const pa_params* p);
+
+/* q           FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned.
+ * k_pages     E4M3 bytes, addressed through the strides in *p (8-byte aligned).
+ * v_pages     E4M3 bytes, same.
+ * block_table int32 [batch][max_pages_per_req]; entries past ceil(L/page_size) are never read.
+ * ctx_lens    int32 [batch]; 0 marks an empty or padded slot.
+ * k_scale     one FP32 in device memory: a K element is E4M3(byte) * *k_scale.
+ * v_scale     one FP32 in device memory: a V element is E4M3(byte) * *v_scale.
+ *             (Device pointers, so a captured graph can be replayed with new scales.)
+ * out         FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned; fully written.
+ * workspace   device buffer of at least pa_decode_fp8_workspace_bytes(p) bytes, 256-byte aligned;
+ *             two calls in flight at the same time must use different workspaces.
+ * stream      cudaStream_t (NULL = legacy default stream).
+ * QK^T and PV run on the tensor cores with FP16 inputs and FP32 accumulation
+ * ("SM70 attention and quantized projection coverage across TP sizes", section
+ * "Scope": FP16 inputs with FP32 accumulation for both QK and PV).
+ * Returns PA_OK after enqueueing the kernels, or a negative pa_status. */
+int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                  const float* v_scale, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- BF16 Q/K/V, head_dim 128 ----------------------------------------------
+ *
+ * The head-dim-128 BF16 decode with group packing ("perf(fa2): port decode GQA
+ * group-swap into d128 varlen launcher", vllm.cpp pull request #48,
+ * description: the query heads of one KV group are packed together, the grid
+ * runs over (batch, kv_heads), and the split count is chosen on the packed
+ * geometry).  Same conventions as pa_decode_fp8 with BF16 elements (2 bytes),
+ * no scales, and softmax scale 1/sqrt(128).
+ * lse         optional (NULL to skip) FP32 [batch][q_len][num_q_heads], 16-byte aligned:
+ *             natural-log log-sum-exp of the row's scores, -inf for a row with no key. */
+size_t pa_decode_bf16_d128_workspace_bytes(const pa_params* p);
+
+int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- status word ------------------------------------------------------------
+ * pa_read_status synchronises `stream`, then copies the status word of
+ * `workspace` to *flags (host).  pa_clear_status enqueues a reset of it. */
+int pa_read_status(const void* workspace, uint32_t* flags, void* stream);
+int pa_clear_status(void* workspace, void* stream);
+
+/* ---- bookkeeping checks -------------------------------------------------------
+ * pa_debug_worklist runs the kernels' own device-side split planner over
+ * ctx_lens and writes, for every work item the split kernel would execute,
+ * one int4 {request, kv_head, key_begin, key_end} into items (device,
+ * capacity max_items) in the order the persistent CTAs take them, and the
+ * item count into *count (device int32).  Returns PA_ERR_SHAPE if max_items
+ * is too small for max_ctx_len.
+ *
+ * pa_debug_gather_fp8 reads, through the kernels' own block-table addressing,
+ * the K (which = 0) or V (which = 1) bytes of every visible key of request b
+ * and KV head g, and writes them densely as dst[b][g][j][256] (device,
+ * [batch][num_kv_heads][max_ctx_len][256] bytes); slots past ctx_lens[b] are
+ * left untouched. */
+int pa_debug_worklist(const pa_params* p, const int32_t* ctx_lens, int32_t* items, int32_t max_items,
+                      int32_t* count, void* stream);
+int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* ctx_lens, int32_t which, void* dst,
+                        void* stream);
+
+/* ---- kernel timing ------------------------------------------------------------
+ * pa_timing_enable(1) makes every later decode call record CUDA events around
+ * its split-KV kernel and its combine kernel (on the call's stream);
+ * pa_timing_collect synchronises those events and returns, for kernel
+ * 0 = split-KV and 1 = combine, the summed device time in milliseconds and
+ * the number of launches timed since the previous collect, then resets them.
+ * Recording stops while disabled.  At most 4096 launches are kept. */
+int pa_timing_enable(int on);
+int pa_timing_collect(int kernel, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

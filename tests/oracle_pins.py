@@ -1,0 +1,256 @@
+"""Pins that tie the FP64 oracle to something other than itself.
+
+Each pin takes a loaded oracle library and returns a list of failure messages
+(empty = pass), so the same pins run against the real oracle and against
+deliberately mutated builds (tests/test_oracle_pins.py checks that every planted
+mistake is caught by at least one pin).
+
+What pins what:
+  * element decoders  - every E4M3 / FP16 / BF16 code against torch / numpy casts,
+                        the E4M3 closed form, and the OCP format points in
+                        tests/golden/e4m3_format_points.txt;
+  * whole definition  - brute force on tiny paged inputs against float64
+                        torch.nn.functional.scaled_dot_product_attention with an
+                        explicit causal mask (an independent library routine);
+  * invariants        - uniform scores give the mean of the visible V and
+                        lse = log(n); a single visible key returns that key's V;
+                        permuting pages together with the block table changes
+                        nothing; zero-length rows are exact zeros even when Q is
+                        NaN; two keys give sigmoid weights; one-hot V rows expose
+                        exactly which keys each verify query sees.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from helpers import dense_reference, run_oracle, visible
+from paged_gqa_decode_split_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e4m3_format_points.txt")
+
+
+def _cmp(name, got, want, atol=0.0, rtol=0.0):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    same = (np.isnan(got) & np.isnan(want)) | (got == want)
+    with np.errstate(invalid="ignore"):
+        close = np.abs(got - want) <= atol + rtol * np.abs(want)
+    bad = ~same & ~close
+    if bad.any():
+        i = int(np.flatnonzero(bad.ravel())[0])
+        return [f"{name}: {int(bad.sum())} mismatches, first at {i}: got {got.ravel()[i]!r} want {want.ravel()[i]!r}"]
+    return []
+
+
+def pin_e4m3_vs_torch(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return _cmp("e4m3 vs torch float8_e4m3fn", oracle.e4m3_value(codes, lib), want)
+
+
+def pin_e4m3_closed_form(lib):
+    want = []
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            v = math.nan
+        elif e == 0:
+            v = m * 2.0 ** -9                 # subnormal: m/8 * 2^-6
+        else:
+            v = (8 + m) * 2.0 ** (e - 10)     # (1 + m/8) * 2^(e-7)
+        want.append(-v if s else v)
+    return _cmp("e4m3 closed form", oracle.e4m3_value(np.arange(256), lib), want)
+
+
+def pin_e4m3_golden(lib):
+    codes, vals = [], []
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            c, v = line.split()
+            codes.append(int(c, 16))
+            vals.append(float(v))
+    got = oracle.e4m3_value(codes, lib)
+    out = _cmp("e4m3 OCP format points", got, vals)
+    # the sign of zero is part of the format
+    for c, g in zip(codes, got):
+        if c in (0x00, 0x80) and math.copysign(1.0, g) != (-1.0 if c == 0x80 else 1.0):
+            out.append(f"e4m3 code {c:#x} has the wrong zero sign")
+    return out
+
+
+def pin_f16_vs_numpy(lib):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    return _cmp("fp16 vs numpy", oracle.f16_value(bits, lib), bits.view(np.float16).astype(np.float64))
+
+
+def pin_bf16_vs_torch(lib):
+    bits = np.arange(65536, dtype=np.int32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    return _cmp("bf16 vs torch", oracle.bf16_value(bits, lib), want)
+
+
+def _tiny(kind, seed, lens, *, Hkv=2, group=3, q_len=4, page_size=16, D=None, layout="separate", base_pad=0):
+    spec = wl.small_spec(kind, batch=len(lens), num_kv_heads=Hkv, group=group, q_len=q_len, page_size=page_size,
+                         max_ctx_len=max(max(lens), 1), layout=layout, base_pad=base_pad, head_dim=D)
+    return wl.generate(spec, seed, ctx_lens=lens)
+
+
+def _bruteforce(lib, kind, **kw):
+    fails = []
+    for seed, lens in ((11, [37, 5, 2, 0]), (12, [16, 33, 1])):
+        w = _tiny(kind, seed, lens, **kw)
+        got, glse = run_oracle(w, lib=lib, num_threads=1)
+        ref, rlse = dense_reference(w)
+        vis = visible(w)
+        fails += _cmp(f"{kind} brute force out (seed {seed})", got[vis], ref[vis], atol=1e-12, rtol=1e-12)
+        fails += _cmp(f"{kind} brute force lse (seed {seed})", glse[vis], rlse[vis], atol=1e-12, rtol=1e-12)
+        if np.any(got[~vis] != 0.0) or np.any(glse[~vis] != -np.inf):
+            fails.append(f"{kind}: rows without keys must be zeros / -inf")
+    return fails
+
+
+def pin_bruteforce_fp8(lib):
+    return _bruteforce(lib, "fp8") + _bruteforce(lib, "fp8", Hkv=1, group=6, q_len=8, layout="interleaved",
+                                                 base_pad=8)
+
+
+def pin_bruteforce_bf16(lib):
+    return _bruteforce(lib, "bf16", Hkv=2, group=4, q_len=1)
+
+
+def pin_uniform_mean(lib):
+    """Q = 0 makes every score 0: out is the mean of the visible V, lse = log(n)."""
+    w = _tiny("fp8", 21, [29, 8, 3], Hkv=2, group=3, q_len=4)
+    w.q.zero_()
+    got, lse = run_oracle(w, lib=lib, num_threads=1)
+    fails = []
+    for b, L in enumerate(w.ctx_lens.tolist()):
+        for g in range(2):
+            from helpers import _elements
+            V = _elements(w, "v", b, g, L).numpy()
+            for qi in range(4):
+                n = L - 4 + qi + 1
+                if n <= 0:
+                    continue
+                for h in range(3 * g, 3 * g + 3):
+                    fails += _cmp(f"uniform mean b{b} qi{qi} h{h}", got[b, qi, h], V[:n].mean(0), atol=1e-13)
+                    fails += _cmp(f"uniform lse b{b} qi{qi} h{h}", lse[b, qi, h], math.log(n), atol=1e-13)
+    return fails
+
+
+def pin_single_key(lib):
+    """With L = q_len, verify query 0 sees exactly key 0 and must return its V."""
+    from helpers import _elements
+    w = _tiny("fp8", 31, [4, 4], Hkv=2, group=3, q_len=4)
+    got, _ = run_oracle(w, lib=lib, num_threads=1)
+    fails = []
+    for b in range(2):
+        for g in range(2):
+            v0 = _elements(w, "v", b, g, 1).numpy()[0]
+            for h in range(3 * g, 3 * g + 3):
+                fails += _cmp(f"single key b{b} h{h}", got[b, 0, h], v0, atol=0.0)
+    return fails
+
+
+def pin_permutation(lib):
+    """Moving pages in the pool and rewriting the block table to match leaves
+    every output bit unchanged."""
+    w = _tiny("fp8", 41, [45, 20], Hkv=2, group=3, q_len=4)
+    base, _ = run_oracle(w, lib=lib, num_threads=1)
+    s = w.spec
+    npg = w.num_pages
+    perm = torch.randperm(npg, generator=torch.Generator().manual_seed(5))   # new slot of old page p
+    region = npg * s.page_size * s.num_kv_heads * s.head_dim
+    kv = w.kv.clone()
+    for old in range(npg):
+        new = int(perm[old])
+        for off in (w.k_offset, w.v_offset):
+            src = off + old * w.k_strides[0]
+            dst = off + new * w.k_strides[0]
+            kv[dst:dst + w.k_strides[0]] = w.kv[src:src + w.k_strides[0]]
+    bt = w.block_table.clone()
+    m = bt >= 0
+    bt[m] = perm[bt[m].long()].to(torch.int32)
+    assert region == w.v_offset - w.k_offset
+    w2 = wl.Workload(**{**w.__dict__, "kv": kv, "block_table": bt})
+    got, _ = run_oracle(w2, lib=lib, num_threads=1)
+    if not np.array_equal(got, base):
+        return ["page permutation changed the output"]
+    return []
+
+
+def pin_zero_length(lib):
+    w = _tiny("fp8", 51, [0, 9, 0], Hkv=2, group=3, q_len=4)
+    w.q[0] = float("nan")
+    w.q[2] = float("nan")
+    got, lse = run_oracle(w, lib=lib, num_threads=1)
+    fails = []
+    for b in (0, 2):
+        if not (np.all(got[b] == 0.0) and np.all(np.signbit(got[b]) == False) and np.all(lse[b] == -np.inf)):
+            fails.append(f"zero-length request {b} must give +0.0 and lse -inf")
+    if not np.all(np.isfinite(got[1])):
+        fails.append("a live request next to NaN-padded slots must stay finite")
+    return fails
+
+
+def pin_two_key(lib):
+    """q_len 1, L 2: out = sigmoid(s0 - s1) v0 + sigmoid(s1 - s0) v1."""
+    from helpers import _elements
+    w = _tiny("fp8", 61, [2, 2], Hkv=1, group=2, q_len=1)
+    got, lse = run_oracle(w, lib=lib, num_threads=1)
+    fails = []
+    D = w.spec.head_dim
+    for b in range(2):
+        K = _elements(w, "k", b, 0, 2).numpy()
+        V = _elements(w, "v", b, 0, 2).numpy()
+        for h in range(2):
+            q = w.q[b, 0, h].double().numpy()
+            s0, s1 = q @ K[0] / math.sqrt(D), q @ K[1] / math.sqrt(D)
+            a0 = 1.0 / (1.0 + math.exp(s1 - s0))
+            a1 = 1.0 / (1.0 + math.exp(s0 - s1))
+            fails += _cmp(f"two-key b{b} h{h}", got[b, 0, h], a0 * V[0] + a1 * V[1], atol=1e-12, rtol=1e-12)
+            fails += _cmp(f"two-key lse b{b} h{h}", lse[b, 0, h], max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))),
+                          atol=1e-12)
+    return fails
+
+
+def pin_causal_window(lib):
+    """BF16 V rows set to one-hot e_j and Q = 0: verify query qi must return
+    1/n on exactly coordinates 0..n-1 with n = L - q_len + qi + 1."""
+    spec = wl.small_spec("bf16", batch=2, num_kv_heads=1, group=2, q_len=5, page_size=16, max_ctx_len=40,
+                         head_dim=64)
+    w = wl.generate(spec, 71, ctx_lens=[37, 3])
+    w.q.zero_()
+    s = spec
+    kv = w.kv.clone()
+    bt = w.block_table
+    for b, L in enumerate(w.ctx_lens.tolist()):
+        for j in range(L):
+            page = int(bt[b, j // s.page_size])
+            start = w.v_offset + page * w.v_strides[0] + (j % s.page_size) * w.v_strides[1]
+            row = torch.zeros(s.head_dim, dtype=torch.bfloat16)
+            row[j] = 1.0
+            kv[start:start + 2 * s.head_dim] = row.view(torch.uint8)
+    w = wl.Workload(**{**w.__dict__, "kv": kv})
+    got, _ = run_oracle(w, lib=lib, num_threads=1)
+    fails = []
+    for b, L in enumerate(w.ctx_lens.tolist()):
+        for qi in range(s.q_len):
+            n = L - s.q_len + qi + 1
+            want = np.zeros(s.head_dim)
+            if n > 0:
+                want[:n] = 1.0 / n
+            for h in range(2):
+                fails += _cmp(f"causal window b{b} qi{qi} h{h}", got[b, qi, h], want, atol=1e-15)
+    return fails
+
+
+ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
+            pin_bruteforce_fp8, pin_bruteforce_bf16, pin_uniform_mean, pin_single_key, pin_permutation,
+            pin_zero_length, pin_two_key, pin_causal_window]
