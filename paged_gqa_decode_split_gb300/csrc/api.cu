@@ -1,0 +1,312 @@
+// C ABI of libpa (declared in include/pa.h): host-side validation, workspace
+// layout, launches and the timing / bookkeeping helpers.  No device memory is
+// allocated here; every buffer belongs to the caller.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kernels.cuh"
+#include "pa.h"
+#include "plan.cuh"
+
+namespace {
+
+using namespace pa;
+
+constexpr int kMaxDevices = 64;
+
+int sm_count(int dev) {
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Geometry checks shared by both variants.  *R receives G * q_len.
+int check_geometry(const pa_params* p, int head_dim, int* R) {
+  if (p == nullptr) return PA_ERR_NULL;
+  if (p->head_dim != head_dim) return PA_ERR_UNSUPPORTED;
+  if (p->batch < 1 || p->batch > kMaxBatch) return PA_ERR_SHAPE;
+  if (p->num_kv_heads < 1 || p->num_q_heads < 1 || p->num_q_heads % p->num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  if (G > kMaxGroup) return PA_ERR_UNSUPPORTED;
+  if (p->q_len < 1 || p->q_len > kMaxQLen) return PA_ERR_SHAPE;
+  if (G * p->q_len > kMaxRows) return PA_ERR_UNSUPPORTED;
+  if (p->page_size <= 0 || p->page_size % kPageMultiple != 0) return PA_ERR_SHAPE;
+  if (p->max_ctx_len < 0 || p->max_ctx_len > kMaxCtx) return PA_ERR_SHAPE;
+  if (p->num_pages < 1 || p->max_pages_per_req < 1) return PA_ERR_SHAPE;
+  if ((long long)p->max_pages_per_req * p->page_size < (long long)p->max_ctx_len) return PA_ERR_SHAPE;
+  const long long st[6] = {p->k_page_stride, p->k_token_stride, p->k_head_stride,
+                           p->v_page_stride, p->v_token_stride, p->v_head_stride};
+  for (long long s : st) {
+    if (s < 0) return PA_ERR_SHAPE;
+    if (s % 8 != 0) return PA_ERR_ALIGN;
+  }
+  *R = G * p->q_len;
+  return PA_OK;
+}
+
+size_t workspace_bytes(const pa_params* p, int head_dim) {
+  int R = 0;
+  if (check_geometry(p, head_dim, &R) != PA_OK) return 0;
+  return ws_layout(p->batch, p->num_kv_heads, max_splits_for(p->max_ctx_len), R, head_dim).total;
+}
+
+bool strides16(const pa_params* p, const void* k, const void* v) {
+  return aligned(k, 16) && aligned(v, 16) && p->k_page_stride % 16 == 0 && p->k_token_stride % 16 == 0 &&
+         p->k_head_stride % 16 == 0 && p->v_page_stride % 16 == 0 && p->v_token_stride % 16 == 0 &&
+         p->v_head_stride % 16 == 0;
+}
+
+// ---- kernel timing ----------------------------------------------------------
+struct Timing {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool[2];  // event pairs per kernel kind: [2*i], [2*i+1]
+  size_t used[2] = {0, 0};
+};
+Timing& timing() {
+  static Timing t;
+  return t;
+}
+constexpr size_t kMaxTimed = 4096;
+
+// Returns the two events to record around one launch of kernel `kind`, or
+// {nullptr, nullptr} when timing is off or full.
+void timing_slot(int kind, cudaEvent_t* a, cudaEvent_t* b) {
+  *a = *b = nullptr;
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  if (!T.on || T.used[kind] >= kMaxTimed) return;
+  auto& pool = T.pool[kind];
+  if (pool.size() < 2 * (T.used[kind] + 1)) {
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess) return;
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+      cudaEventDestroy(e0);
+      return;
+    }
+    pool.push_back(e0);
+    pool.push_back(e1);
+  }
+  *a = pool[2 * T.used[kind]];
+  *b = pool[2 * T.used[kind] + 1];
+  T.used[kind]++;
+}
+
+int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
+                  void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr) {
+  const int D = bf16 ? 128 : 256;
+  int R = 0;
+  int st = check_geometry(p, D, &R);
+  if (st != PA_OK) return st;
+  if (!q || !k_pages || !v_pages || !block_table || !ctx_lens || !out) return PA_ERR_NULL;
+  if (!bf16 && (!k_scale || !v_scale)) return PA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PA_ERR_ALIGN;
+  if (!aligned(k_pages, 8) || !aligned(v_pages, 8) || !aligned(block_table, 4) || !aligned(ctx_lens, 4))
+    return PA_ERR_ALIGN;
+  if (!bf16 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return PA_ERR_ALIGN;
+  const int s_max = max_splits_for(p->max_ctx_len);
+  const WsLayout L = ws_layout(p->batch, p->num_kv_heads, s_max, R, D);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes_given < L.total) return PA_ERR_WORKSPACE;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  const int nsm = sm_count(dev);
+  if (nsm <= 0) return PA_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* bad = reinterpret_cast<uint32_t*>(ws + kWsBadOff);
+  if (cudaMemsetAsync(bad, 0, sizeof(uint32_t) * p->batch, stream) != cudaSuccess) return PA_ERR_CUDA;
+
+  SplitArgs a;
+  a.q = q;
+  a.k = static_cast<const uint8_t*>(k_pages);
+  a.v = static_cast<const uint8_t*>(v_pages);
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.k_scale = k_scale;
+  a.panel_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  a.panel_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.status = status;
+  a.bad = bad;
+  a.k_ps = p->k_page_stride, a.k_ts = p->k_token_stride, a.k_hs = p->k_head_stride;
+  a.v_ps = p->v_page_stride, a.v_ts = p->v_token_stride, a.v_hs = p->v_head_stride;
+  a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;
+  a.q_len = p->q_len, a.R = R, a.page_size = p->page_size, a.mpr = p->max_pages_per_req;
+  a.num_pages = p->num_pages, a.max_ctx = p->max_ctx_len, a.s_max = s_max;
+
+  const long long max_items = (long long)p->batch * p->num_kv_heads * (s_max > 0 ? s_max : 1);
+  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  cudaEvent_t e0, e1;
+  timing_slot(0, &e0, &e1);
+  if (e0) cudaEventRecord(e0, stream);
+  if (launch_split(a, bf16, grid, strides16(p, k_pages, v_pages), stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (e1) cudaEventRecord(e1, stream);
+
+  CombineArgs c;
+  c.ctx_lens = ctx_lens;
+  c.panel_ml = a.panel_ml;
+  c.panel_o = a.panel_o;
+  c.bad = bad;
+  c.out_scale_ptr = bf16 ? nullptr : v_scale;
+  c.out_scale_mul = bf16 ? 1.0f : kE4m3Unscale;
+  c.out = out;
+  c.lse = lse;
+  c.B = a.B, c.Hkv = a.Hkv, c.Hq = a.Hq, c.G = a.G, c.q_len = a.q_len, c.R = R, c.D = D;
+  c.max_ctx = a.max_ctx, c.s_max = s_max;
+  timing_slot(1, &e0, &e1);
+  if (e0) cudaEventRecord(e0, stream);
+  if (launch_combine(c, bf16, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (e1) cudaEventRecord(e1, stream);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_get_capabilities(pa_caps* out) {
+  if (out == nullptr) return PA_ERR_NULL;
+  std::memset(out, 0, sizeof(*out));
+  out->abi_version = PA_ABI_VERSION;
+  out->max_batch = kMaxBatch;
+  out->max_q_len = kMaxQLen;
+  out->max_group = kMaxGroup;
+  out->page_multiple = kPageMultiple;
+  out->max_ctx = kMaxCtx;
+  out->accum_bits = 32;
+  out->fp8_head_dim = 256;
+  out->bf16_head_dim = 128;
+  return PA_OK;
+}
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_SHAPE: return "shape, length, page size or stride out of range";
+    case PA_ERR_UNSUPPORTED: return "unsupported head_dim or GQA geometry";
+    case PA_ERR_ALIGN: return "pointer or stride not aligned as required";
+    case PA_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
+    case PA_ERR_CUDA: return "CUDA runtime or launch failure";
+    default: return "unknown status";
+  }
+}
+
+int pa_split_plan(int32_t ctx_len, int32_t* num_splits, int32_t* chunk) {
+  if (!num_splits || !chunk) return PA_ERR_NULL;
+  if (ctx_len < 0) return PA_ERR_SHAPE;
+  int s, c;
+  split_plan(ctx_len, s, c);
+  *num_splits = s;
+  *chunk = c;
+  return PA_OK;
+}
+
+size_t pa_decode_fp8_workspace_bytes(const pa_params* p) { return workspace_bytes(p, 256); }
+size_t pa_decode_bf16_d128_workspace_bytes(const pa_params* p) { return workspace_bytes(p, 128); }
+
+int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
+                  void* out, void* workspace, size_t workspace_bytes_given, void* stream) {
+  return decode_common(false, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
+                       workspace, workspace_bytes_given, stream);
+}
+
+int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes_given, void* stream) {
+  return decode_common(true, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, lse, workspace,
+                       workspace_bytes_given, stream);
+}
+
+int pa_read_status(const void* workspace, uint32_t* flags, void* stream) {
+  if (!workspace || !flags) return PA_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_clear_status(void* workspace, void* stream) {
+  if (!workspace) return PA_ERR_NULL;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_debug_worklist(const pa_params* p, const int32_t* ctx_lens, int32_t* items, int32_t max_items,
+                      int32_t* count, void* stream) {
+  if (!p || !ctx_lens || !items || !count) return PA_ERR_NULL;
+  if (p->batch < 1 || p->batch > kMaxBatch || p->num_kv_heads < 1) return PA_ERR_SHAPE;
+  if (p->max_ctx_len < 0 || p->max_ctx_len > kMaxCtx) return PA_ERR_SHAPE;
+  const long long need = (long long)p->batch * p->num_kv_heads * max_splits_for(p->max_ctx_len);
+  if (max_items < need) return PA_ERR_SHAPE;
+  // invalid lengths are planned as 0 here too; the decode calls report them
+  if (launch_debug_worklist(ctx_lens, p->batch, p->num_kv_heads, p->max_ctx_len, items, max_items, count,
+                            nullptr, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                        const int32_t* ctx_lens, int32_t which, void* dst, void* stream) {
+  int R = 0;
+  int st = check_geometry(p, 256, &R);
+  if (st != PA_OK) return st;
+  if (!k_pages || !v_pages || !block_table || !ctx_lens || !dst) return PA_ERR_NULL;
+  if (which != 0 && which != 1) return PA_ERR_SHAPE;
+  const uint8_t* base = static_cast<const uint8_t*>(which == 0 ? k_pages : v_pages);
+  const long long ps = which == 0 ? p->k_page_stride : p->v_page_stride;
+  const long long ts = which == 0 ? p->k_token_stride : p->v_token_stride;
+  const long long hs = which == 0 ? p->k_head_stride : p->v_head_stride;
+  if (launch_debug_gather(base, ps, ts, hs, block_table, ctx_lens, p->batch, p->num_kv_heads, p->page_size,
+                          p->max_pages_per_req, p->num_pages, p->max_ctx_len, 256, static_cast<uint8_t*>(dst),
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_timing_enable(int on) {
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  T.on = on != 0;
+  return PA_OK;
+}
+
+int pa_timing_collect(int kernel, double* total_ms, int64_t* launches) {
+  if (!total_ms || !launches) return PA_ERR_NULL;
+  if (kernel != 0 && kernel != 1) return PA_ERR_SHAPE;
+  Timing& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  double sum = 0.0;
+  for (size_t i = 0; i < T.used[kernel]; ++i) {
+    cudaEvent_t a = T.pool[kernel][2 * i], b = T.pool[kernel][2 * i + 1];
+    if (cudaEventSynchronize(b) != cudaSuccess) return PA_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return PA_ERR_CUDA;
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = (int64_t)T.used[kernel];
+  T.used[kernel] = 0;
+  return PA_OK;
+}
+
+}  // extern "C"

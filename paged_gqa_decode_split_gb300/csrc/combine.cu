@@ -1,0 +1,128 @@
+// Log-sum-exp combine of the split partials, plus the bookkeeping check kernels.
+//
+// For one output row (request b, KV head g, packed row r = qi * G + hl) with
+// splits s = 0 .. S-1 in ascending order ("perf(fa2): port decode GQA
+// group-swap into d128 varlen launcher", vllm.cpp pull request #48: the
+// num_splits > 1 path merges split partials with their log-sum-exp):
+//   M = max_s m_s,  w_s = 2^(m_s - M),  out = scale * sum_s w_s O_s / sum_s w_s l_s
+// with m in log2 units.  A row with no visible key anywhere (M = -inf), a
+// request of length 0 and a request flagged by an input check all write +0.0.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "plan.cuh"
+#include "kernels.cuh"
+
+namespace pa {
+
+namespace {
+
+template <bool BF16OUT>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  const int row = blockIdx.x % a.R;
+  const int bg = blockIdx.x / a.R;
+  const int g = bg % a.Hkv;
+  const int b = bg / a.Hkv;
+  const int qi = row / a.G, hl = row % a.G;
+  int L = a.ctx_lens[b];
+  if (L < 0 || L > a.max_ctx) L = 0;
+  int ns, chunk;
+  split_plan(L, ns, chunk);
+  const bool bad = a.bad != nullptr && a.bad[b] != 0u;
+  const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
+  const size_t prow = (size_t)bg * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
+  float M = -INFINITY;
+  if (!bad)
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.panel_ml[prow + (size_t)s * a.R].x);
+  float lsum = 0.f;
+  if (M != -INFINITY)
+    for (int s = 0; s < ns; ++s) {
+      const float2 ml = a.panel_ml[prow + (size_t)s * a.R];
+      const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+      lsum += w * ml.y;
+    }
+  const float scale = (a.out_scale_ptr ? __ldg(a.out_scale_ptr) : 1.0f) * a.out_scale_mul;
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    float val = 0.f;
+    if (M != -INFINITY && lsum > 0.f) {
+      float acc = 0.f;
+      for (int s = 0; s < ns; ++s) {
+        const size_t pr = prow + (size_t)s * a.R;
+        const float2 ml = a.panel_ml[pr];
+        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        acc += w * a.panel_o[pr * a.D + d];
+      }
+      val = acc / lsum * scale;
+    }
+    if constexpr (BF16OUT) {
+      reinterpret_cast<__nv_bfloat16*>(a.out)[orow * a.D + d] = __float2bfloat16_rn(val);
+    } else {
+      reinterpret_cast<__half*>(a.out)[orow * a.D + d] = __float2half_rn(val);
+    }
+  }
+  if (a.lse != nullptr && threadIdx.x == 0) {
+    a.lse[orow] = (M == -INFINITY || !(lsum > 0.f)) ? -INFINITY : (M + log2f(lsum)) * 0.6931471805599453f;
+  }
+}
+
+__global__ void __launch_bounds__(64) worklist_kernel(const int32_t* ctx_lens, int B, int Hkv, int max_ctx,
+                                                      int32_t* items, int32_t max_items, int32_t* count,
+                                                      uint32_t* status) {
+  __shared__ Sched S;
+  sched_build(S, ctx_lens, B, Hkv, max_ctx, status, nullptr);
+  if (threadIdx.x == 0) *count = S.total;
+  for (int it = threadIdx.x; it < S.total && it < max_items; it += blockDim.x) {
+    const Item x = sched_item(S, B, it);
+    items[4 * it + 0] = x.b;
+    items[4 * it + 1] = x.g;
+    items[4 * it + 2] = x.t0;
+    items[4 * it + 3] = x.t1;
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(const uint8_t* base, long long ps, long long ts, long long hs,
+                                                     const int32_t* bt, const int32_t* ctx_lens, int Hkv,
+                                                     int page_size, int mpr, int num_pages, int max_ctx,
+                                                     int row_bytes, uint8_t* dst) {
+  const int bg = blockIdx.x;
+  const int b = bg / Hkv, g = bg % Hkv;
+  int L = ctx_lens[b];
+  if (L < 0 || L > max_ctx) L = 0;
+  const int32_t* bt_row = bt + (size_t)b * mpr;
+  for (int t = blockIdx.y; t < L; t += gridDim.y) {
+    const long long off = kv_row_offset(bt_row, t, page_size, num_pages, ps, ts);
+    if (off < 0) continue;
+    const uint8_t* src = base + (long long)g * hs + off;
+    uint8_t* out = dst + ((size_t)bg * max_ctx + t) * row_bytes;
+    for (int c = threadIdx.x; c < row_bytes; c += blockDim.x) out[c] = src[c];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream) {
+  const int grid = a.B * a.Hkv * a.R;
+  const int threads = a.D < 256 ? a.D : 256;
+  if (bf16_out)
+    combine_kernel<true><<<grid, threads, 0, stream>>>(a);
+  else
+    combine_kernel<false><<<grid, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
+                                  int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream) {
+  worklist_kernel<<<1, 64, 0, stream>>>(ctx_lens, B, Hkv, max_ctx, items, max_items, count, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gather(const uint8_t* base, long long ps, long long ts, long long hs, const int32_t* bt,
+                                const int32_t* ctx_lens, int B, int Hkv, int page_size, int mpr, int num_pages,
+                                int max_ctx, int row_bytes, uint8_t* dst, cudaStream_t stream) {
+  dim3 grid(B * Hkv, 64);
+  gather_kernel<<<grid, 256, 0, stream>>>(base, ps, ts, hs, bt, ctx_lens, Hkv, page_size, mpr, num_pages, max_ctx,
+                                          row_bytes, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,46 @@
+// Launch interface of the kernels behind pa.h (internal to libpa).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Split-KV kernel arguments (both element formats).
+struct SplitArgs {
+  const void* q;               // FP16 (E4M3 path) or BF16 (BF16 path) [B][q_len][Hq][D]
+  const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs
+  const uint8_t* v;
+  const int32_t* block_table;  // [B][mpr]
+  const int32_t* ctx_lens;     // [B]
+  const float* k_scale;        // E4M3 path only
+  float2* panel_ml;            // (m in log2 units, l) per (item, row)
+  float* panel_o;              // unnormalised O per (item, row, d); E4M3 path: times 2^-8, no v_scale
+  uint32_t* status;
+  uint32_t* bad;
+  long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
+  int B, Hkv, Hq, G, q_len, R, page_size, mpr, num_pages, max_ctx, s_max;
+};
+
+struct CombineArgs {
+  const int32_t* ctx_lens;
+  const float2* panel_ml;
+  const float* panel_o;
+  const uint32_t* bad;
+  const float* out_scale_ptr;  // nullable: output is multiplied by *out_scale_ptr * out_scale_mul
+  float out_scale_mul;
+  void* out;                   // FP16 (E4M3 path) or BF16 (BF16 path)
+  float* lse;                  // nullable
+  int B, Hkv, Hq, G, q_len, R, D, max_ctx, s_max;
+};
+
+int split_smem_bytes();
+cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, bool vec16, cudaStream_t stream);
+cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream);
+cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
+                                  int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_debug_gather(const uint8_t* base, long long ps, long long ts, long long hs, const int32_t* bt,
+                                const int32_t* ctx_lens, int B, int Hkv, int page_size, int mpr, int num_pages,
+                                int max_ctx, int row_bytes, uint8_t* dst, cudaStream_t stream);
+
+}  // namespace pa

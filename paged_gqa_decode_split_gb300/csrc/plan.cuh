@@ -1,0 +1,164 @@
+// Split planning, the persistent work schedule, the workspace layout and the
+// E4M3 decode shared by the kernels of libpa.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// ------------------------------------------------------------ constants --
+constexpr int kTileKeys = 128;     // keys per tensor-core tile (MMA M dimension)
+constexpr int kSplitTarget = 512;  // a split holds about this many keys before the cap
+constexpr int kMaxSplits = 32;     // at most this many splits per request
+constexpr int kMaxBatch = 64;
+constexpr int kMaxQLen = 8;
+constexpr int kMaxGroup = 8;
+constexpr int kMaxRows = 64;       // G * q_len rows of one packed tile
+constexpr int kPageMultiple = 16;
+constexpr int kMaxCtx = 1 << 20;
+
+// Split plan of one request of L keys.  It depends on L alone, never on the
+// batch, so a request produces the same partials (and the combine the same
+// bits) whether it runs alone or next to others.  Splits are whole tiles of
+// kTileKeys keys except the last; every split is non-empty.
+__host__ __device__ inline void split_plan(int L, int& num_splits, int& chunk) {
+  if (L <= 0) {
+    num_splits = 0;
+    chunk = 0;
+    return;
+  }
+  int s0 = (L + kSplitTarget - 1) / kSplitTarget;
+  s0 = s0 < 1 ? 1 : (s0 > kMaxSplits ? kMaxSplits : s0);
+  int per = (L + s0 - 1) / s0;
+  chunk = (per + kTileKeys - 1) / kTileKeys * kTileKeys;
+  num_splits = (L + chunk - 1) / chunk;
+}
+
+__host__ __device__ inline int max_splits_for(int max_ctx_len) {
+  int s, c;
+  split_plan(max_ctx_len, s, c);
+  return s;
+}
+
+// ------------------------------------------------------------ workspace --
+// [0, 4)          status word (PA_FLAG_* bits, sticky)
+// [512, 768)      per-request "bad input" flags (cleared by the host API each call)
+// [1024, ...)     panel_ml: float2 (m, l) [B][Hkv][S_max][R]
+// [...]           panel_o : float      [B][Hkv][S_max][R][D]   (unnormalised partial O)
+struct WsLayout {
+  size_t ml_off, o_off, total;
+};
+__host__ __device__ inline WsLayout ws_layout(int B, int Hkv, int s_max, int R, int D) {
+  WsLayout w;
+  size_t items = (size_t)B * Hkv * (size_t)s_max * R;
+  w.ml_off = 1024;
+  w.o_off = (w.ml_off + items * 8 + 255) / 256 * 256;
+  w.total = (w.o_off + items * (size_t)D * 4 + 255) / 256 * 256;
+  return w;
+}
+constexpr size_t kWsBadOff = 512;
+
+// ------------------------------------------------------------- schedule --
+// Every CTA derives the same ordered item list from ctx_lens: requests sorted
+// by split length (longest first, ties by request index), then KV head, then
+// split.  CTA c executes items c, c + gridDim.x, ...  The order only balances
+// work; each item's arithmetic and output slot depend on (b, g, s) alone.
+struct Sched {
+  int total;                 // number of items
+  int order[kMaxBatch];      // request index of the o-th request in schedule order
+  int first[kMaxBatch + 1];  // first item of the o-th request
+  int nsplit[kMaxBatch];     // splits of request b (by request index)
+  int chunk[kMaxBatch];      // split length of request b
+  int len[kMaxBatch];        // validated length of request b (0 if invalid)
+};
+
+struct Item {
+  int b, g, s, t0, t1, L;
+};
+
+// Called by every thread of the CTA (uses __syncthreads).  Invalid lengths
+// (< 0 or > max_ctx) count as 0 and raise PA_FLAG_BAD_LENGTH once (CTA 0).
+__device__ inline void sched_build(Sched& S, const int32_t* ctx_lens, int B, int Hkv, int max_ctx,
+                                   uint32_t* status, uint32_t* bad) {
+  int t = threadIdx.x;
+  if (t < B) {
+    int L = ctx_lens[t];
+    if (L < 0 || L > max_ctx) {
+      if (blockIdx.x == 0) {
+        if (status) atomicOr(status, 0x2u);
+        if (bad) atomicOr(bad + t, 1u);
+      }
+      L = 0;
+    }
+    int ns, ch;
+    split_plan(L, ns, ch);
+    S.len[t] = L;
+    S.nsplit[t] = ns;
+    S.chunk[t] = ch;
+  }
+  __syncthreads();
+  if (t == 0) {
+    for (int i = 0; i < B; ++i) S.order[i] = i;
+    for (int i = 1; i < B; ++i) {  // insertion sort: chunk descending, index ascending
+      int v = S.order[i], j = i - 1;
+      while (j >= 0 && S.chunk[S.order[j]] < S.chunk[v]) {
+        S.order[j + 1] = S.order[j];
+        --j;
+      }
+      S.order[j + 1] = v;
+    }
+    int acc = 0;
+    for (int o = 0; o < B; ++o) {
+      S.first[o] = acc;
+      acc += S.nsplit[S.order[o]] * Hkv;
+    }
+    S.first[B] = acc;
+    S.total = acc;
+  }
+  __syncthreads();
+}
+
+__device__ inline Item sched_item(const Sched& S, int B, int it) {
+  int o = 0;
+  while (o + 1 < B && S.first[o + 1] <= it) ++o;
+  int b = S.order[o];
+  int local = it - S.first[o];
+  int ns = S.nsplit[b];
+  Item x;
+  x.b = b;
+  x.g = local / ns;
+  x.s = local % ns;
+  x.L = S.len[b];
+  x.t0 = x.s * S.chunk[b];
+  int e = x.t0 + S.chunk[b];
+  x.t1 = e < x.L ? e : x.L;
+  return x;
+}
+
+// Byte offset of key t's row (relative to the KV-head base) through the block
+// table, or -1 when the page id is outside [0, num_pages).  Shared by the
+// split kernels' loaders and the bookkeeping check kernel.
+__device__ __forceinline__ long long kv_row_offset(const int32_t* bt_row, int t, int page_size, int num_pages,
+                                                   long long page_stride, long long token_stride) {
+  const int page = __ldg(bt_row + t / page_size);
+  if ((unsigned)page >= (unsigned)num_pages) return -1;
+  return (long long)page * page_stride + (long long)(t % page_size) * token_stride;
+}
+
+// ------------------------------------------------------------ E4M3 -> FP16 --
+// An E4M3 code (sign s, exponent e, mantissa m) placed as FP16 bits
+// s.0eeee.mmm0000000 is exactly E4M3 * 2^-8 for every finite code, normal or
+// subnormal (same 3-bit mantissa, exponent bias 7 vs 15).  Both formats are
+// public definitions (OCP E4M3, IEEE binary16); the 2^8 goes into the scales.
+// x holds four codes (byte 0 = lowest index); lo receives codes 0,1 and hi
+// codes 2,3 as FP16x2 (lower index in the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  uint32_t w0 = __byte_perm(x, 0u, 0x1404u);  // [c1 0 c0 0]
+  uint32_t w1 = __byte_perm(x, 0u, 0x3424u);  // [c3 0 c2 0]
+  lo = (w0 & 0x80008000u) | ((w0 >> 1) & 0x3FFF3FFFu);
+  hi = (w1 & 0x80008000u) | ((w1 >> 1) & 0x3FFF3FFFu);
+}
+constexpr float kE4m3Unscale = 256.0f;  // undo the 2^-8 of the decode above
+
+}  // namespace pa

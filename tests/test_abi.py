@@ -1,0 +1,175 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every entry
+point include/pa.h declares, reports its capabilities, plans splits as the
+restatement below does, sizes workspaces, and rejects every bad argument
+before touching CUDA."""
+import ctypes
+import math
+
+import pytest
+
+from paged_gqa_decode_split_gb300 import binding as B
+from paged_gqa_decode_split_gb300 import build as pa_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return B.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = B.header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+
+
+def test_capabilities(lib):
+    c = B.pa_get_capabilities()
+    assert c.abi_version == 1
+    assert c.accum_bits == 32
+    assert c.page_multiple == 16
+    assert c.fp8_head_dim == 256 and c.bf16_head_dim == 128
+    assert c.max_q_len >= 8 and c.max_group >= 6 and c.max_batch >= 16 and c.max_ctx >= 262144
+    assert lib.pa_get_capabilities(None) == B.PA_ERR_NULL
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, 42):
+        assert isinstance(B.status_string(code), str) and B.status_string(code)
+
+
+def splits_for_len(L: int) -> tuple[int, int]:
+    """Restatement of the split policy: about 512 keys per split, at most 32
+    splits, split length a whole number of 128-key tiles."""
+    if L <= 0:
+        return 0, 0
+    s0 = min(max(math.ceil(L / 512), 1), 32)
+    chunk = math.ceil(math.ceil(L / s0) / 128) * 128
+    return math.ceil(L / chunk), chunk
+
+
+@pytest.mark.parametrize("L", [0, 1, 7, 8, 127, 128, 129, 511, 512, 513, 3297, 16383, 32768, 131072, 131073,
+                               200000, 262144, 1 << 20])
+def test_split_plan_matches_restatement(lib, L):
+    st, s, c = B.pa_split_plan(L)
+    assert st == 0
+    assert (s, c) == splits_for_len(L)
+    if L > 0:
+        assert 1 <= s <= 32 and c % 128 == 0
+        assert (s - 1) * c < L <= s * c  # every split non-empty
+
+
+def test_split_plan_rejects_negative(lib):
+    assert B.pa_split_plan(-1)[0] == B.PA_ERR_SHAPE
+
+
+def test_split_plan_known_configs(lib):
+    assert B.pa_split_plan(131072)[1:] == (32, 4096)
+    assert B.pa_split_plan(3297)[1:] == (7, 512)
+    assert B.pa_split_plan(262144)[1:] == (32, 8192)
+
+
+def _params(**kw):
+    base = dict(batch=8, num_kv_heads=1, num_q_heads=6, head_dim=256, q_len=8, page_size=1648,
+                max_pages_per_req=80, num_pages=640, max_ctx_len=131072, k_strides=(1648 * 256, 256, 256),
+                v_strides=(1648 * 256, 256, 256))
+    base.update(kw)
+    return B.make_params(**base)
+
+
+def test_workspace_size_formula(lib):
+    p = _params()
+    n = B.pa_decode_fp8_workspace_bytes(p)
+    items = 8 * 1 * 32 * 48
+    assert n >= 1024 + items * 8 + items * 256 * 4
+    assert n % 256 == 0
+    assert B.pa_decode_fp8_workspace_bytes(_params(head_dim=128)) == 0
+    q = _params(head_dim=128, num_kv_heads=8, num_q_heads=32, q_len=1, page_size=16, max_pages_per_req=2048,
+                max_ctx_len=32768, k_strides=(16 * 8 * 256, 8 * 256, 256), v_strides=(16 * 8 * 256, 8 * 256, 256))
+    assert B.pa_decode_bf16_d128_workspace_bytes(q) >= 1024 + 8 * 8 * 32 * 4 * (128 * 4 + 8)
+
+
+FAKE = 0x10000  # 64 KiB-aligned fake device address: never dereferenced, every check fails first
+
+
+def _call(p, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, ks=FAKE, vs=FAKE, out=FAKE, ws=FAKE,
+                ws_bytes=1 << 40)
+    args.update(over)
+    return B.pa_decode_fp8(p, args["q"], args["k"], args["v"], args["bt"], args["cl"], args["ks"], args["vs"],
+                           args["out"], args["ws"], args["ws_bytes"], 0)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(head_dim=128), B.PA_ERR_UNSUPPORTED),
+    (dict(batch=0), B.PA_ERR_SHAPE),
+    (dict(batch=65), B.PA_ERR_SHAPE),
+    (dict(q_len=0), B.PA_ERR_SHAPE),
+    (dict(q_len=9), B.PA_ERR_SHAPE),
+    (dict(num_kv_heads=2, num_q_heads=7), B.PA_ERR_SHAPE),   # heads not a multiple of KV heads
+    (dict(num_kv_heads=0), B.PA_ERR_SHAPE),
+    (dict(num_q_heads=18), B.PA_ERR_UNSUPPORTED),            # GQA 18 > max_group
+    (dict(page_size=1000), B.PA_ERR_SHAPE),
+    (dict(page_size=0), B.PA_ERR_SHAPE),
+    (dict(max_pages_per_req=10), B.PA_ERR_SHAPE),
+    (dict(max_ctx_len=-1), B.PA_ERR_SHAPE),
+    (dict(max_ctx_len=(1 << 20) + 1, max_pages_per_req=1 << 20), B.PA_ERR_SHAPE),
+    (dict(num_pages=0), B.PA_ERR_SHAPE),
+], ids=lambda x: str(x))
+def test_rejects_bad_geometry(lib, over, expect):
+    assert _call(_params(**over)) == expect
+
+
+def test_rejects_misaligned_strides(lib):
+    assert _call(_params(k_strides=(1648 * 256, 260, 256))) == B.PA_ERR_ALIGN
+    assert _call(_params(v_strides=(1648 * 256, 256, -256))) == B.PA_ERR_SHAPE
+
+
+@pytest.mark.parametrize("arg", ["q", "k", "v", "bt", "cl", "ks", "vs", "out"])
+def test_rejects_null_pointers(lib, arg):
+    assert _call(_params(), **{arg: 0}) == B.PA_ERR_NULL
+
+
+def test_rejects_misaligned_pointers(lib):
+    assert _call(_params(), q=FAKE + 8) == B.PA_ERR_ALIGN
+    assert _call(_params(), out=FAKE + 2) == B.PA_ERR_ALIGN
+    assert _call(_params(), k=FAKE + 4) == B.PA_ERR_ALIGN
+
+
+def test_rejects_bad_workspace(lib):
+    p = _params()
+    need = B.pa_decode_fp8_workspace_bytes(p)
+    assert _call(p, ws=0) == B.PA_ERR_WORKSPACE
+    assert _call(p, ws=FAKE + 128) == B.PA_ERR_WORKSPACE
+    assert _call(p, ws_bytes=need - 1) == B.PA_ERR_WORKSPACE
+
+
+def test_null_params(lib):
+    assert lib.pa_decode_fp8(None, *([ctypes.c_void_p(FAKE)] * 9), 1 << 30, None) == B.PA_ERR_NULL
+    assert lib.pa_decode_fp8_workspace_bytes(None) == 0
+
+
+def test_bf16_entry_validates(lib):
+    p = _params(head_dim=128, num_kv_heads=8, num_q_heads=32, q_len=1, page_size=16, max_pages_per_req=2048,
+                max_ctx_len=32768, k_strides=(16 * 8 * 256, 8 * 256, 256), v_strides=(16 * 8 * 256, 8 * 256, 256))
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, out=FAKE, lse=None, ws=FAKE, n=1 << 40)
+
+    def call(**o):
+        a = {**ok, **o}
+        return B.pa_decode_bf16_d128(p, a["q"], a["k"], a["v"], a["bt"], a["cl"], a["out"], a["lse"], a["ws"],
+                                     a["n"], 0)
+    assert call(q=0) == B.PA_ERR_NULL
+    assert call(lse=FAKE + 4) == B.PA_ERR_ALIGN
+    assert call(n=0) == B.PA_ERR_WORKSPACE
+    p.head_dim = 256
+    assert call() == B.PA_ERR_UNSUPPORTED
+
+
+def test_timing_and_status_arguments(lib):
+    assert B.pa_timing_enable(False) == 0
+    assert B.pa_timing_collect(2)[0] == B.PA_ERR_SHAPE
+    st, ms, n = B.pa_timing_collect(0)
+    assert st == 0 and n == 0 and ms == 0.0
+    assert lib.pa_read_status(None, None, None) == B.PA_ERR_NULL
+    assert lib.pa_clear_status(None, None) == B.PA_ERR_NULL

@@ -1,0 +1,311 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Small cases are compared row by row in full (several 128-key tiles, ragged
+tails, every q_len, GQA up to 8, several KV heads, 8-byte-only aligned
+interleaved K/V, zero-length and padded slots, contexts shorter than the verify
+window); the five workload configurations are run at full size in the same
+launch configuration the benchmark uses and compared on all rows where the
+oracle is affordable, otherwise on sampled rows."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import check_full, check_rows, to_f64
+from paged_gqa_decode_split_gb300 import binding as B
+from paged_gqa_decode_split_gb300 import build as pa_build
+from paged_gqa_decode_split_gb300 import decode as D
+from paged_gqa_decode_split_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pa_build.build()
+    B.load()
+
+
+def _small(kind, lens, *, Hkv=1, group=6, q_len=8, page_size=16, layout="separate", base_pad=0, seed=1,
+           max_ctx=None, padded=()):
+    D_ = 256 if kind == "fp8" else 128
+    spec = wl.Spec(f"small_{kind}", kind, len(lens), Hkv, Hkv * group, D_, q_len, page_size,
+                   max_ctx or max(max(lens), 1), ctx_lens=tuple(lens), padded_slots=tuple(padded), layout=layout,
+                   base_pad=base_pad)
+    return wl.generate(spec, seed).to("cuda")
+
+
+SMALL = [
+    # id, kind, lens, kwargs
+    ("fp8_tiles_tail", "fp8", [300, 37], {}),
+    ("fp8_hkv2_interleaved_8B", "fp8", [700, 129, 0], dict(Hkv=2, page_size=32, layout="interleaved", base_pad=8)),
+    ("fp8_q1", "fp8", [1000, 5], dict(q_len=1)),
+    ("fp8_q2", "fp8", [513, 2], dict(q_len=2)),
+    ("fp8_q3", "fp8", [257, 40], dict(q_len=3)),
+    ("fp8_q5_hkv3", "fp8", [384, 128], dict(q_len=5, Hkv=3)),
+    ("fp8_g8_q8", "fp8", [513, 64], dict(group=8)),
+    ("fp8_g4_q4", "fp8", [640, 11], dict(group=4, q_len=4)),
+    ("fp8_short_contexts", "fp8", [1, 2, 7, 8, 9, 16, 0], {}),
+    ("fp8_page48_many_splits", "fp8", [20000, 4097], dict(page_size=48)),
+    ("fp8_padded_nan", "fp8", [900, 0, 33, 0], dict(padded=(3,))),
+    ("bf16_d128", "bf16", [1500, 2048, 17], dict(Hkv=8, group=4, q_len=1)),
+    ("bf16_d128_q4_8B", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="interleaved", base_pad=8)),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_against_oracle(case):
+    _, kind, lens, kw = case
+    w = _small(kind, lens, **kw)
+    dec = D.Decoder(w, with_lse=(kind == "bf16"))
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out, dec.lse)
+
+
+# ----------------------------------------------------------- full-size configs --
+
+def _full(name, w_index=0):
+    spec = wl.SPECS[name]
+    return wl.generate(spec, wl.working_set_seed(name, w_index), device="cuda")
+
+
+def test_config_b1_l3297():
+    w = _full("b1_l3297")
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+
+
+def test_config_b4_l32k():
+    w = _full("b4_l32k", 3)
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+
+
+def _sample_rows(w, per_request: int, seed: int) -> np.ndarray:
+    s = w.spec
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(s.batch):
+        base = b * s.q_len * s.num_q_heads
+        # always the first and last verify query of the first and last head, plus random ones
+        fixed = [base, base + s.num_q_heads - 1, base + (s.q_len - 1) * s.num_q_heads,
+                 base + s.q_len * s.num_q_heads - 1]
+        rnd = rng.integers(0, s.q_len * s.num_q_heads, per_request) + base
+        rows.extend(fixed + list(rnd))
+    return np.unique(np.array(rows, dtype=np.int32))
+
+
+def test_config_b8_l128k_sampled():
+    w = _full("b8_l128k")
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_rows(w, dec.out, _sample_rows(w, 2, 5))
+    assert torch.isfinite(dec.out.float()).all()
+
+
+def test_config_b16_mixed_sampled():
+    w = _full("b16_mixed")
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    out = dec.out
+    lens = w.ctx_lens.cpu().tolist()
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[b] == 0) and not torch.signbit(out[b].float()).any()
+    # the longest and the shortest live request in full, the rest sampled
+    live = [b for b, L in enumerate(lens) if L > 0]
+    longest, shortest = max(live, key=lambda b: lens[b]), min(live, key=lambda b: lens[b])
+    s = w.spec
+    per = s.q_len * s.num_q_heads
+    rows = set(range(longest * per, (longest + 1) * per)) | set(range(shortest * per, (shortest + 1) * per))
+    rows |= set(_sample_rows(w, 1, 9).tolist())
+    check_rows(w, out, np.array(sorted(rows), dtype=np.int32))
+
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8])
+def test_config_d128(b):
+    w = _full(f"d128_b{b}")
+    dec = D.Decoder(w, with_lse=True)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out, dec.lse)
+
+
+# ------------------------------------------------------------ invariants --
+
+def _single(w, b):
+    """Request b of workload w as a batch of one (same KV buffer and pool)."""
+    s = w.spec
+    spec1 = wl.Spec(s.name + "_single", s.kind, 1, s.num_kv_heads, s.num_q_heads, s.head_dim, s.q_len,
+                    s.page_size, s.max_ctx_len, ctx_lens=(0,), layout=s.layout, base_pad=s.base_pad)
+    return wl.Workload(spec=spec1, q=w.q[b:b + 1].clone(), kv=w.kv, k_offset=w.k_offset, v_offset=w.v_offset,
+                       k_strides=w.k_strides, v_strides=w.v_strides, block_table=w.block_table[b:b + 1].clone(),
+                       ctx_lens=w.ctx_lens[b:b + 1].clone(), num_pages=w.num_pages, k_scale=w.k_scale,
+                       v_scale=w.v_scale)
+
+
+@pytest.mark.parametrize("name", ["b4_l32k", "b16_mixed", "d128_b8"])
+def test_batched_equals_single_bitwise(name):
+    w = _full(name)
+    batched = D.Decoder(w).run().clone()
+    for b in range(w.spec.batch):
+        one = D.Decoder(_single(w, b)).run()
+        assert torch.equal(one[0].view(torch.int16), batched[b].view(torch.int16)), f"request {b} differs"
+
+
+def test_graph_replay_with_changed_inputs():
+    w = _full("b4_l32k", 1)
+    dec = D.Decoder(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.check(dec(s), "warm-up")
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.check(dec(torch.cuda.current_stream()), "captured call")
+    g.replay()
+    torch.cuda.synchronize()
+    ref1 = D.Decoder(w).run().clone()
+    assert torch.equal(dec.out.view(torch.int16), ref1.view(torch.int16))
+    # change Q, lengths (including a zero row) and scales in place, replay
+    w.q.copy_(torch.randn_like(w.q.float()).half())
+    w.ctx_lens.copy_(torch.tensor([32768, 77, 0, 20001], dtype=torch.int32))
+    dec.scales.mul_(1.5)
+    g.replay()
+    torch.cuda.synchronize()
+    w2 = wl.Workload(**{**w.__dict__, "k_scale": float(dec.scales[0]), "v_scale": float(dec.scales[1])})
+    ref2 = D.Decoder(w2).run().clone()
+    assert torch.equal(dec.out.view(torch.int16), ref2.view(torch.int16))
+    check_full(w2, dec.out)
+
+
+# ---------------------------------------------------------- bookkeeping --
+
+def schedule(lens, Hkv):
+    """Restatement of the persistent schedule: requests by split length
+    descending (ties by index), then KV head, then split."""
+    plans = []
+    for L in lens:
+        st, s, c = B.pa_split_plan(max(L, 0))
+        plans.append((s, c))
+    order = sorted(range(len(lens)), key=lambda b: (-plans[b][1], b))
+    items = []
+    for b in order:
+        s, c = plans[b]
+        for g in range(Hkv):
+            for k in range(s):
+                items.append((b, g, k * c, min((k + 1) * c, lens[b])))
+    return items
+
+
+def test_worklist_bit_exact():
+    lens = [131072, 0, 3297, 262144, 1, 129, 77777, 0, 8]
+    spec = wl.Spec("wl", "fp8", len(lens), 2, 12, 256, 8, 3296, 262144, ctx_lens=tuple(lens))
+    w = wl.generate(spec, 3)
+    p = D.params_for(w)
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    cap = len(lens) * 2 * 32
+    items = torch.full((cap, 4), -7, dtype=torch.int32, device="cuda")
+    count = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.check(B.pa_debug_worklist(p, cl, items, cap, count), "pa_debug_worklist")
+    torch.cuda.synchronize()
+    want = schedule(lens, 2)
+    assert int(count) == len(want)
+    assert [tuple(r) for r in items[:len(want)].cpu().tolist()] == want
+
+
+@pytest.mark.parametrize("layout,pad", [("separate", 0), ("interleaved", 8)])
+def test_gather_bit_exact(layout, pad):
+    lens = [3297, 1, 0, 2000]
+    spec = wl.Spec("ga", "fp8", len(lens), 2, 12, 256, 8, 1648, 4000, ctx_lens=tuple(lens), layout=layout,
+                   base_pad=pad)
+    w = wl.generate(spec, 4).to("cuda")
+    p = D.params_for(w)
+    kv = w.kv.data_ptr()
+    for which, off, st in ((0, w.k_offset, w.k_strides), (1, w.v_offset, w.v_strides)):
+        dst = torch.zeros((len(lens), 2, spec.max_ctx_len, 256), dtype=torch.uint8, device="cuda")
+        B.check(B.pa_debug_gather_fp8(p, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens, which, dst),
+                "gather")
+        torch.cuda.synchronize()
+        host = w.kv.cpu().numpy()
+        bt = w.block_table.cpu().numpy()
+        got = dst.cpu().numpy()
+        for b, L in enumerate(lens):
+            for g in range(2):
+                want = np.stack([host[off + bt[b, j // 1648] * st[0] + (j % 1648) * st[1] + g * st[2]:][:256]
+                                 for j in range(L)]) if L else np.zeros((0, 256), np.uint8)
+                assert np.array_equal(got[b, g, :L], want)
+
+
+# ------------------------------------------------------------ input checks --
+
+def test_bad_page_flags_and_zeros_request():
+    w = _small("fp8", [400, 300, 50], page_size=32, seed=7)
+    w.block_table[1, 3] = w.num_pages + 5
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() & B.PA_FLAG_BAD_PAGE
+    assert torch.all(dec.out[1] == 0)
+    from helpers import run_oracle
+    ref, _ = run_oracle(w.to("cpu").__class__(**{**w.to("cpu").__dict__}), rows=np.arange(0, 48, dtype=np.int32))
+    assert np.abs(to_f64(dec.out[0]).reshape(48, 256) - ref).max() <= 2e-3
+    B.check(B.pa_clear_status(dec.workspace), "clear")
+    assert dec.status() == 0
+
+
+def test_bad_length_flags_and_zeros_request():
+    w = _small("fp8", [400, 300], page_size=32, seed=8, max_ctx=512)
+    w.ctx_lens[0] = 513  # beyond max_ctx_len
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() & B.PA_FLAG_BAD_LENGTH
+    assert torch.all(dec.out[0] == 0)
+    w.ctx_lens[0] = -3
+    B.check(B.pa_clear_status(dec.workspace), "clear")
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() & B.PA_FLAG_BAD_LENGTH
+    assert torch.all(dec.out[0] == 0)
+
+
+# ------------------------------------------------------ online-softmax rescale --
+
+def test_growing_scores_force_rescales():
+    """Scores that grow along the context move each row's running maximum by
+    far more than the lazy threshold many times (the O^T rescale path)."""
+    lens = [2000, 700]
+    w = _small("fp8", lens, page_size=16, seed=11)
+    s = w.spec
+    w.q.fill_(1.0)
+    # K row of key j: every element the E4M3 code of a value growing with j
+    codes = torch.tensor([0x20 + (j * 0x5B) // 2000 for j in range(max(lens))], dtype=torch.uint8)
+    kv = w.kv.cpu()
+    bt = w.block_table.cpu()
+    for b, L in enumerate(lens):
+        for j in range(L):
+            page = int(bt[b, j // s.page_size])
+            start = w.k_offset + page * w.k_strides[0] + (j % s.page_size) * w.k_strides[1]
+            kv[start:start + 256] = codes[j]
+    w = wl.Workload(**{**w.__dict__, "kv": kv.cuda(), "k_scale": 0.02})
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
