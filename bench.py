@@ -1,0 +1,408 @@
+"""Benchmark: paged GQA verify-decode attention, B8 x 131072 keys, E4M3 K/V.
+
+One step = one pa_decode_fp8 call (split-KV kernel + log-sum-exp combine) over
+one batch: 8 requests, 131072-token contexts, page 1648, 1 KV head, GQA 6,
+q_len 8, head_dim 256, FP16 Q, E4M3 K/V with per-tensor FP32 scales.  Steps
+rotate over 16 per-layer KV working sets (536,870,912 unique KV bytes each, so
+every step's inputs are far larger than the 129 MB L2; no flush is needed).
+
+Printed JSON (one line, rank 0):
+  value      effective KV GB/s = unique KV bytes of all steps on all ranks / max
+             wall time over ranks (CUDA events, inputs resident in HBM)
+  roofline   split-kernel achieved GB/s (algorithmic unique KV bytes / its own
+             average launch time, CUDA events around every launch) vs the
+             measured HBM copy bandwidth
+  e2e        the same metric through the C ABI with pinned host buffers: each
+             step copies its inputs host->device and reads the output back
+  cpu_baseline  the FP64 oracle on a bounded sample, on this host's cores
+
+--impl reference times the oracle itself as the comparison arm.
+Multi-GPU (torchrun): independent replicas, one per rank (no data-path
+collective); the barrier and the max over ranks use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "b8_l128k"
+METRIC = "µs per decode-attention call and effective KV GB/s (% of HBM peak) @B8/128K"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kernel_b8_l128k_traffic.json")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return None, 0, 1, 0
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    dist.init_process_group("gloo")
+    return dist, rank, ws, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_split_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic():
+    """DRAM bytes per split-kernel launch from the committed ncu capture, or
+    None when absent or taken on a different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(t["dram_bytes_per_launch_full"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- oracle --
+
+def _oracle_rate(w, rows, threads=0):
+    """Time the FP64 oracle on the given flat rows of workload w (host copy);
+    returns (seconds, threads used)."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    lib = oracle.load()
+    nthreads = threads or oracle.max_threads(lib)
+    q_bits = w.q.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.paged_attn(w.spec.kind, q=q_bits, kv=w.kv.numpy(), k_offset=w.k_offset, v_offset=w.v_offset,
+                      k_strides=w.k_strides, v_strides=w.v_strides, block_table=w.block_table.numpy(),
+                      ctx_lens=w.ctx_lens.numpy(), num_kv_heads=w.spec.num_kv_heads, page_size=w.spec.page_size,
+                      k_scale=w.k_scale, v_scale=w.v_scale, rows=np.asarray(rows, np.int32), num_threads=nthreads,
+                      lib=lib)
+    return time.perf_counter() - t0, nthreads
+
+
+def cpu_baseline_sample(w_cpu, seconds_target=15.0):
+    """Oracle on whole rows of request 0 (full 131072-key context), as many rows
+    as fit the time target; returns the cpu_baseline dict."""
+    spec = w_cpu.spec
+    per_row = 2 * spec.head_dim * spec.elem_bytes * spec.num_kv_heads / (spec.num_q_heads * spec.q_len)
+    import oracle
+
+    nthreads = oracle.max_threads()
+    L = int(w_cpu.ctx_lens[0])
+    t1, _ = _oracle_rate(w_cpu, list(range(nthreads)), nthreads)  # calibration: one row per thread
+    rows_total = spec.q_len * spec.num_q_heads
+    rounds = max(1, min(rows_total // nthreads, int(seconds_target / max(t1, 1e-3))))
+    nrows = min(rows_total, rounds * nthreads)
+    t, used = _oracle_rate(w_cpu, list(range(nrows)), nthreads)
+    keys = sum(max(0, L - spec.q_len + (r // spec.num_q_heads) + 1) for r in range(nrows))
+    value = keys * per_row / t / 1e9
+    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"{nrows} of {spec.batch * rows_total} output rows (request 0, full {L}-key context), "
+                      f"{t:.2f} s; GB/s counts {per_row:.3f} unique-KV bytes per (row, visible key)"}
+
+
+# --------------------------------------------------------------------- arms --
+
+def describe(spec) -> str:
+    return (f"B{spec.batch} x {spec.max_ctx_len}-token contexts, page {spec.page_size}, Hkv {spec.num_kv_heads}, "
+            f"Hq {spec.num_q_heads} (GQA {spec.num_q_heads // spec.num_kv_heads}), q_len {spec.q_len}, "
+            f"D {spec.head_dim}, " + ("FP16 Q, E4M3 K/V per-tensor scales" if spec.kind == "fp8" else "BF16 Q/K/V")
+            + ", random block table")
+
+
+def reduce_max(values, dist):
+    """Element-wise max of a list of floats over all ranks (no-op on one rank)."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def run_reference(args, rank, world):
+    """The comparison arm: the FP64 oracle itself, on host cores."""
+    from paged_gqa_decode_split_gb300 import workloads as wl
+
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    spec = wl.SPECS[args.workload]
+    w = wl.generate(spec, wl.working_set_seed(args.workload, 0), device="cpu")
+    nthreads = oracle.max_threads()
+    per_row = 2 * spec.head_dim * spec.elem_bytes * spec.num_kv_heads / (spec.num_q_heads * spec.q_len)
+    # each step: one row per thread over a prefix of request 0, sized so the run fits ~2 minutes
+    budget = 120.0 / (args.steps + args.warmup)
+    t_full, _ = _oracle_rate(w, list(range(nthreads)), nthreads)
+    L = int(w.ctx_lens[0])
+    n_keys = int(min(L, max(256, L * budget / max(t_full, 1e-6))))
+    w_s = wl.Workload(**{**w.__dict__, "ctx_lens": w.ctx_lens.clone().fill_(n_keys)})
+    rows = list(range(nthreads))
+    for _ in range(args.warmup):
+        _oracle_rate(w_s, rows, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_rate(w_s, rows, nthreads)
+    dt = time.perf_counter() - t0
+    keys = sum(max(0, n_keys - spec.q_len + (r // spec.num_q_heads) + 1) for r in rows)
+    value = keys * per_row * args.steps / dt / 1e9
+    sample = (f"per step {len(rows)} output rows of request 0 over its first {n_keys} keys; GB/s counts "
+              f"{per_row:.3f} unique-KV bytes per (row, visible key)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(spec), "global_batch": spec.batch, "seq_len": spec.max_ctx_len,
+                       "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, dist, rank, world, local):
+    import torch
+
+    from paged_gqa_decode_split_gb300 import binding as B
+    from paged_gqa_decode_split_gb300 import build as pa_build
+    from paged_gqa_decode_split_gb300 import decode as D
+    from paged_gqa_decode_split_gb300 import workloads as wl
+
+    if rank == 0 or not pa_build.up_to_date():
+        pa_build.build()
+    if dist is not None:
+        dist.barrier()
+    B.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    spec = wl.SPECS[name]
+    nsets = args.working_sets
+    sets = [wl.generate(spec, wl.working_set_seed(name, w) + 1000 * rank, device=dev) for w in range(nsets)]
+    decs = [D.Decoder(w) for w in sets]
+    unique = sets[0].unique_kv_bytes()
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        B.check(decs[i % nsets](stream), "warm-up call")
+    torch.cuda.synchronize(dev)
+    for d in decs:
+        if d.status() != 0:
+            raise RuntimeError(f"status flags {d.status():#x} after warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first readings
+    B.pa_timing_collect(0)
+    B.pa_timing_collect(1)
+    B.pa_timing_enable(True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        B.check(decs[i % nsets](stream), "timed call")
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    B.pa_timing_enable(False)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    st0, split_ms, split_n = B.pa_timing_collect(0)
+    st1, comb_ms, comb_n = B.pa_timing_collect(1)
+    for d in decs:
+        if d.status() != 0:
+            raise RuntimeError(f"status flags {d.status():#x} after the timed region")
+
+    # e2e through the C ABI with pinned host buffers
+    host = wl.generate(spec, wl.working_set_seed(name, 0) + 1000 * rank, device=dev).to("cpu")
+    hq, hkv = host.q.pin_memory(), host.kv.pin_memory()
+    hbt, hcl = host.block_table.pin_memory(), host.ctx_lens.pin_memory()
+    hsc = torch.tensor([host.k_scale, host.v_scale], dtype=torch.float32).pin_memory()
+    hout = torch.empty_like(host.q).pin_memory()
+    dw = wl.Workload(**{**host.__dict__, "q": torch.empty_like(hq, device=dev), "kv": torch.empty_like(hkv, device=dev),
+                        "block_table": torch.empty_like(hbt, device=dev), "ctx_lens": torch.empty_like(hcl, device=dev)})
+    e2e_dec = D.Decoder(dw)
+    h2d = hq.nbytes + hkv.nbytes + hbt.nbytes + hcl.nbytes + hsc.nbytes
+    d2h = hout.nbytes
+
+    def e2e_step():
+        dw.q.copy_(hq, non_blocking=True)
+        dw.kv.copy_(hkv, non_blocking=True)
+        dw.block_table.copy_(hbt, non_blocking=True)
+        dw.ctx_lens.copy_(hcl, non_blocking=True)
+        e2e_dec.scales.copy_(hsc, non_blocking=True)
+        B.check(e2e_dec(stream), "e2e call")
+        hout.copy_(e2e_dec.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = args.e2e_steps
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    ref_out = D.Decoder(wl.generate(spec, wl.working_set_seed(name, 0) + 1000 * rank, device=dev)).run()
+    torch.cuda.synchronize(dev)
+    if not torch.equal(hout.to(dev).view(torch.int16), ref_out.view(torch.int16)):
+        raise RuntimeError("e2e output differs from the device-resident call")
+
+    ms, e2e_s = reduce_max([ms, e2e_s], dist)
+    if rank != 0:
+        return
+
+    peak, peak_kind = _peaks()
+    total_bytes = unique * args.steps * world
+    value = total_bytes / (ms / 1e3) / 1e9
+    split_avg_s = split_ms / max(split_n, 1) / 1e3
+    achieved = unique / split_avg_s / 1e9
+    traffic = _traffic()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(host)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "us_per_call": ms / args.steps * 1e3,
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xe4m3->f32",
+        "data": "synthetic",
+        "config": {"workload": describe(spec),
+                   "global_batch": spec.batch * world, "seq_len": spec.max_ctx_len,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "working_sets": nsets, "l2": "no flush: every step's KV (537 MB) exceeds the 129 MB L2",
+                   "unique_kv_bytes_per_call": unique},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "split-KV kernel (pa_decode_fp8 main kernel)",
+                     "kernel_avg_us": split_avg_s * 1e6, "combine_avg_us": comb_ms / max(comb_n, 1) * 1e3,
+                     "timed_launches": split_n},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": unique * e_steps * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "note": "pinned host -> device copy of Q, K/V pages, block table, lengths and scales, the call, "
+                        "and a device -> host read of the output, synchronised every step"},
+        "cpu_baseline": cpu,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, help="workload name (default: the B8/128K metric config)")
+    ap.add_argument("--working-sets", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    dist, rank, world, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, dist, rank, world, local)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "plan.cuh"
 #include "ptx.cuh"
 #include "kernels.cuh"
@@ -688,8 +690,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
 template <class Fmt, int NM, int VEC>
 cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
   auto kern = split_kernel<Fmt, NM, VEC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the attribute is per device; setting it is idempotent, so a racing second
+  // setter is harmless
+  static std::atomic<uint64_t> set_on_devices{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(set_on_devices.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    set_on_devices.fetch_or(bit);
+  }
   kern<<<grid, kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
