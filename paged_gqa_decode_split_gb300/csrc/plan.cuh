@@ -35,10 +35,13 @@ __host__ __device__ inline void split_plan(int L, int& num_splits, int& chunk) {
   num_splits = (L + chunk - 1) / chunk;
 }
 
+// Upper bound of split_plan's count over every L <= max_ctx_len.  The count
+// itself is not monotone in L (the split length jumps by whole tiles), but it
+// never exceeds clamp(ceil(L / kSplitTarget), 1, kMaxSplits), which is.
 __host__ __device__ inline int max_splits_for(int max_ctx_len) {
-  int s, c;
-  split_plan(max_ctx_len, s, c);
-  return s;
+  if (max_ctx_len <= 0) return 1;
+  int s0 = (max_ctx_len + kSplitTarget - 1) / kSplitTarget;
+  return s0 < 1 ? 1 : (s0 > kMaxSplits ? kMaxSplits : s0);
 }
 
 // ------------------------------------------------------------ workspace --

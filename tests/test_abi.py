@@ -60,6 +60,21 @@ def test_split_plan_matches_restatement(lib, L):
         assert (s - 1) * c < L <= s * c  # every split non-empty
 
 
+def test_split_count_bounded_by_workspace_bound(lib):
+    """The count is not monotone in L (S(16384) = 32, S(16385) = 26), so the
+    workspace is sized with the monotone bound clamp(ceil(max_ctx/512), 1, 32);
+    no length up to max_ctx may need more splits than that."""
+    assert B.pa_split_plan(16384)[1] == 32 and B.pa_split_plan(16385)[1] == 26
+    worst = 0
+    for L in range(0, 70000, 7):
+        worst = max(worst, B.pa_split_plan(L)[1])
+        assert B.pa_split_plan(L)[1] <= min(32, max(1, math.ceil(L / 512)))
+    assert worst == 32
+    # the workspace of max_ctx_len 16385 must hold 32 splits per (request, KV head)
+    p = _params(max_ctx_len=16385, max_pages_per_req=10)
+    assert B.pa_decode_fp8_workspace_bytes(p) >= 1024 + 8 * 32 * 48 * (256 * 4 + 8)
+
+
 def test_split_plan_rejects_negative(lib):
     assert B.pa_split_plan(-1)[0] == B.PA_ERR_SHAPE
 
