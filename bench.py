@@ -166,24 +166,27 @@ def _oracle_rate(w, rows, threads=0):
 
 
 def cpu_baseline_sample(w_cpu, seconds_target=15.0):
-    """Oracle on whole rows of request 0 (full 131072-key context), as many rows
-    as fit the time target; returns the cpu_baseline dict."""
+    """Oracle on whole output rows (full contexts) of the benchmark call, as
+    many rows as fit the time target (all of them if possible); returns the
+    cpu_baseline dict."""
     spec = w_cpu.spec
     per_row = 2 * spec.head_dim * spec.elem_bytes * spec.num_kv_heads / (spec.num_q_heads * spec.q_len)
     import oracle
 
     nthreads = oracle.max_threads()
-    L = int(w_cpu.ctx_lens[0])
+    rows_total = spec.batch * spec.q_len * spec.num_q_heads
     t1, _ = _oracle_rate(w_cpu, list(range(nthreads)), nthreads)  # calibration: one row per thread
-    rows_total = spec.q_len * spec.num_q_heads
     rounds = max(1, min(rows_total // nthreads, int(seconds_target / max(t1, 1e-3))))
     nrows = min(rows_total, rounds * nthreads)
     t, used = _oracle_rate(w_cpu, list(range(nrows)), nthreads)
-    keys = sum(max(0, L - spec.q_len + (r // spec.num_q_heads) + 1) for r in range(nrows))
+    lens = w_cpu.ctx_lens.tolist()
+    per_req = spec.q_len * spec.num_q_heads
+    keys = sum(max(0, lens[r // per_req] - spec.q_len + ((r % per_req) // spec.num_q_heads) + 1)
+               for r in range(nrows))
     value = keys * per_row / t / 1e9
     return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"{nrows} of {spec.batch * rows_total} output rows (request 0, full {L}-key context), "
-                      f"{t:.2f} s; GB/s counts {per_row:.3f} unique-KV bytes per (row, visible key)"}
+            "sample": f"{nrows} of {rows_total} output rows of one call (full contexts), {t:.2f} s wall; "
+                      f"GB/s counts {per_row:.3f} unique-KV bytes per (row, visible key)"}
 
 
 # --------------------------------------------------------------------- arms --

@@ -204,6 +204,16 @@ int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_p
                         const int32_t* block_table, const int32_t* ctx_lens, int32_t which, void* dst,
                         void* stream);
 
+/* ---- wait-bound check --------------------------------------------------------
+ * Test hook for the kernels' bounded waits.  The next pa_decode_* call made in
+ * this process (by any thread) runs its split kernel with every pipeline wait
+ * bounded by wait_limit_cycles SM cycles and never signals that its Q tile is
+ * ready, so the tensor-core issuer's wait runs out: every CTA abandons its
+ * work, frees its tensor memory, sets PA_FLAG_TIMEOUT in the status word and
+ * exits; the output of that call is invalid and the CUDA context stays usable.
+ * Returns PA_ERR_SHAPE if wait_limit_cycles <= 0. */
+int pa_debug_stall_next(int64_t wait_limit_cycles);
+
 /* ---- kernel timing ------------------------------------------------------------
  * pa_timing_enable(1) makes every later decode call record CUDA events around
  * its split-KV kernel and its combine kernel (on the call's stream);

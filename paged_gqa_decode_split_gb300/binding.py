@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
             "pa_clear_status": ([vp, vp], ctypes.c_int),
             "pa_debug_worklist": ([pp, vp, vp, i32, vp, vp], ctypes.c_int),
             "pa_debug_gather_fp8": ([pp, vp, vp, vp, vp, i32, vp, vp], ctypes.c_int),
+            "pa_debug_stall_next": ([i64], ctypes.c_int),
             "pa_timing_enable": ([ctypes.c_int], ctypes.c_int),
             "pa_timing_collect": ([ctypes.c_int, _P(ctypes.c_double), _P(i64)], ctypes.c_int),
         }
@@ -181,6 +182,10 @@ def pa_debug_worklist(p: pa_params, ctx_lens, items, max_items: int, count, stre
 def pa_debug_gather_fp8(p: pa_params, k_pages, v_pages, block_table, ctx_lens, which: int, dst, stream=None) -> int:
     return load().pa_debug_gather_fp8(ctypes.byref(p), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                       _ptr(ctx_lens), int(which), _ptr(dst), _stream(stream))
+
+
+def pa_debug_stall_next(wait_limit_cycles: int) -> int:
+    return load().pa_debug_stall_next(int(wait_limit_cycles))
 
 
 def pa_timing_enable(on: bool) -> int:

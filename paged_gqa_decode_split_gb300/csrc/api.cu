@@ -3,6 +3,7 @@
 // allocated here; every buffer belongs to the caller.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -17,6 +18,10 @@ namespace {
 using namespace pa;
 
 constexpr int kMaxDevices = 64;
+
+// Test hook state (pa_debug_stall_next): the next decode call runs with this
+// wait bound and withholds its Q-ready signal.
+std::atomic<long long> g_stall_next{0};
 
 int sm_count(int dev) {
   static std::mutex mu;
@@ -149,6 +154,9 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;
   a.q_len = p->q_len, a.R = R, a.page_size = p->page_size, a.mpr = p->max_pages_per_req;
   a.num_pages = p->num_pages, a.max_ctx = p->max_ctx_len, a.s_max = s_max;
+  const long long stall = g_stall_next.exchange(0);
+  a.wait_limit = stall > 0 ? stall : 0;
+  a.withhold_q = stall > 0 ? 1 : 0;
 
   const long long max_items = (long long)p->batch * p->num_kv_heads * (s_max > 0 ? s_max : 1);
   const int grid = (int)(max_items < nsm ? max_items : nsm);
@@ -280,6 +288,12 @@ int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_p
                           p->max_pages_per_req, p->num_pages, p->max_ctx_len, 256, static_cast<uint8_t*>(dst),
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_debug_stall_next(int64_t wait_limit_cycles) {
+  if (wait_limit_cycles <= 0) return PA_ERR_SHAPE;
+  g_stall_next.store(wait_limit_cycles);
   return PA_OK;
 }
 

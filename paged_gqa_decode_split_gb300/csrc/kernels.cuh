@@ -20,6 +20,8 @@ struct SplitArgs {
   uint32_t* bad;
   long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
   int B, Hkv, Hq, G, q_len, R, page_size, mpr, num_pages, max_ctx, s_max;
+  long long wait_limit;  // pipeline wait bound in cycles (0: default)
+  int withhold_q;        // test hook: never signal the Q tile, so the MMA wait runs out
 };
 
 struct CombineArgs {

@@ -32,22 +32,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bound on every pipeline wait, in SM clock cycles (about one second at the
-// GB300 clock).  A healthy wait in these kernels takes microseconds; a wait
-// that reaches the bound means a broken pipeline, and the caller abandons the
-// work item, raises the timeout status bit and tears down cleanly.
+// Default bound on every pipeline wait, in SM clock cycles (about one second
+// at the GB300 clock).  A healthy wait in these kernels takes microseconds; a
+// wait that reaches the bound means a broken pipeline, and the caller
+// abandons its work, raises the timeout status bit and tears down cleanly.
 constexpr long long kWaitLimitCycles = 2000000000ll;
 
-// Returns false when the wait timed out or when another role already aborted
-// (*abort != 0).  Never spins without bound.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Per-CTA abort state shared by all roles.
+struct WaitCtl {
+  volatile int abort;
+  long long limit;  // cycles
+};
+
+// Returns false when the wait timed out or when another role already aborted.
+// Never spins without bound.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
+  const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      *abort = 1;
+    if (ctl->abort) return false;
+    if (clock64() - t0 > ctl->limit) {
+      ctl->abort = 1;
       return false;
     }
   }

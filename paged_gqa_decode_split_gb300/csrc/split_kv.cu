@@ -101,7 +101,7 @@ struct Misc {
   uint64_t kbuf_full[2], kbuf_empty[2], s_full[2], s_empty[2], p_full[2], pv_done[2];
   uint64_t vbuf_full, q_full, q_empty, o_free, grp, fin;
   uint32_t tmem_base;
-  int abort;
+  WaitCtl ctl;
   int exceed_tag[2][4];
   int rescale_tag;
   float mref[kMaxRows];
@@ -208,7 +208,7 @@ __device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is
   uint64_t* full = is_v ? M.vst_full : M.kst_full;
   uint64_t* empty = is_v ? M.vst_empty : M.kst_empty;
   uint8_t* ring = smem_base() + (is_v ? kOffVst : kOffKst);
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   uint32_t c = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
@@ -263,7 +263,7 @@ template <class Fmt>
 __device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane) {
   constexpr int kPieces = Fmt::D / 8;  // 16-byte pieces per Q row
   uint8_t* qbuf = smem_base() + kOffQ;
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   const uint16_t* q = reinterpret_cast<const uint16_t*>(a.q);
   uint32_t n = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x, ++n) {
@@ -276,7 +276,12 @@ __device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane
       const uint32_t dst = smem_u32(qbuf + (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
       cp_async_16(dst, src, 16u);
     }
-    cp_async_arrive(&M.q_full);
+    // the tensor core reads Q through the async proxy: land the copies, fence,
+    // then signal
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && !a.withhold_q) mbar_arrive(&M.q_full);  // withheld only by the timeout test hook
   }
   cp_async_wait_all();
 }
@@ -286,7 +291,7 @@ __device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane
 template <class Fmt>
 __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb) {
   uint8_t* ring = smem_base() + kOffKst;
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   uint32_t j = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
@@ -340,7 +345,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
   uint8_t* sm = smem_base();
   uint8_t* ring = sm + kOffVst;
   uint8_t* vbuf = sm + kOffV;
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   uint32_t j = 0;
   const int key = 32 * i + lane;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
@@ -393,7 +398,7 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
   constexpr uint32_t id_pv = idesc_f16(128, NM, 0, 1, 1);
   constexpr int kKSteps = Fmt::D / 16;
   constexpr int kHalves = Fmt::D / 128;
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   uint32_t j = 0, n = 0;
   bool ok = true;
   auto issue_pv = [&](uint32_t jj, bool first) -> bool {
@@ -448,7 +453,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
   constexpr int CNT = BF::Count;
   constexpr int kHalves = Fmt::D / 128;
   uint8_t* pbuf = smem_base() + kOffP;
-  volatile int* abort = &M.abort;
+  WaitCtl* abort = &M.ctl;
   const int gt = 32 * i + lane;  // thread index inside the softmax group
   const float c_log2 = Fmt::score_scale(a.k_scale);
   const uint32_t lane_base = tb + ((uint32_t)(32 * i) << 16);
@@ -632,12 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
       mbar_init(&M.pv_done[s], 1);
     }
     mbar_init(&M.vbuf_full, 4);
-    mbar_init(&M.q_full, 32);
+    mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
     mbar_init(&M.o_free, 4);
     mbar_init(&M.grp, 4);
     mbar_init(&M.fin, 1);
-    M.abort = 0;
+    M.ctl.abort = 0;
+    M.ctl.limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
     M.rescale_tag = 0;
     for (int w = 0; w < 8; ++w) M.exceed_tag[w / 4][w % 4] = 0;
     mbar_fence_init();
@@ -666,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
       // drain: every issued MMA must finish before TMEM is released
       mma_commit(&M.fin);
       const long long t0 = clock64();
-      while (!mbar_try_wait(&M.fin, 0) && clock64() - t0 < kWaitLimitCycles) {
+      while (!mbar_try_wait(&M.fin, 0) && clock64() - t0 < M.ctl.limit) {
       }
     }
     __syncwarp();
@@ -684,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tb, 512);
   }
-  if (tid == 0 && M.abort) atomicOr(a.status, 0x4u);
+  if (tid == 0 && M.ctl.abort) atomicOr(a.status, 0x4u);
 }
 
 template <class Fmt, int NM, int VEC>

@@ -309,3 +309,27 @@ def test_growing_scores_force_rescales():
     torch.cuda.synchronize()
     assert dec.status() == 0
     check_full(w, dec.out)
+
+
+# ------------------------------------------------------------ bounded waits --
+
+def test_wait_bound_runs_out_cleanly():
+    """With the Q-ready signal withheld and a ~10 ms wait bound, every CTA must
+    give up, free its tensor memory and raise PA_FLAG_TIMEOUT; the context
+    stays usable and the next call is correct."""
+    import time
+
+    w = _small("fp8", [3000, 700, 37], seed=21)
+    dec = D.Decoder(w)
+    B.check(B.pa_debug_stall_next(20_000_000), "pa_debug_stall_next")
+    t0 = time.perf_counter()
+    B.check(dec(), "stalled call")
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 30.0
+    assert dec.status() & B.PA_FLAG_TIMEOUT
+    B.check(B.pa_clear_status(dec.workspace), "clear")
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+    assert B.pa_debug_stall_next(0) == B.PA_ERR_SHAPE
