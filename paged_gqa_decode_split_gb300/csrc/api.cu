@@ -172,7 +172,7 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   c.panel_o = a.panel_o;
   c.bad = bad;
   c.out_scale_ptr = bf16 ? nullptr : v_scale;
-  c.out_scale_mul = bf16 ? 1.0f : kE4m3Unscale;
+  c.out_scale_mul = 1.0f;
   c.out = out;
   c.lse = lse;
   c.B = a.B, c.Hkv = a.Hkv, c.Hq = a.Hq, c.G = a.G, c.q_len = a.q_len, c.R = R, c.D = D;

@@ -15,7 +15,7 @@ struct SplitArgs {
   const int32_t* ctx_lens;     // [B]
   const float* k_scale;        // E4M3 path only
   float2* panel_ml;            // (m in log2 units, l) per (item, row)
-  float* panel_o;              // unnormalised O per (item, row, d); E4M3 path: times 2^-8, no v_scale
+  float* panel_o;              // unnormalised O per (item, row, d); E4M3 path: without v_scale
   uint32_t* status;
   uint32_t* bad;
   long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;

@@ -150,18 +150,15 @@ __device__ __forceinline__ long long kv_row_offset(const int32_t* bt_row, int t,
 }
 
 // ------------------------------------------------------------ E4M3 -> FP16 --
-// An E4M3 code (sign s, exponent e, mantissa m) placed as FP16 bits
-// s.0eeee.mmm0000000 is exactly E4M3 * 2^-8 for every finite code, normal or
-// subnormal (same 3-bit mantissa, exponent bias 7 vs 15).  Both formats are
-// public definitions (OCP E4M3, IEEE binary16); the 2^8 goes into the scales.
-// x holds four codes (byte 0 = lowest index); lo receives codes 0,1 and hi
-// codes 2,3 as FP16x2 (lower index in the low half).
-__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  uint32_t w0 = __byte_perm(x, 0u, 0x1404u);  // [c1 0 c0 0]
-  uint32_t w1 = __byte_perm(x, 0u, 0x3424u);  // [c3 0 c2 0]
-  lo = (w0 & 0x80008000u) | ((w0 >> 1) & 0x3FFF3FFFu);
-  hi = (w1 & 0x80008000u) | ((w1 >> 1) & 0x3FFF3FFFu);
+// Every finite E4M3 value (|x| <= 448, subnormals down to 2^-9) is exactly
+// representable in FP16, so the hardware conversion is exact.  x holds four
+// codes (byte 0 = lowest index); lo receives codes 0,1 and hi codes 2,3 as
+// FP16x2 with the lower index in the low half.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
-constexpr float kE4m3Unscale = 256.0f;  // undo the 2^-8 of the decode above
 
 }  // namespace pa

@@ -16,7 +16,7 @@
 // with FP32 accumulators in TMEM ("SM70 attention and quantized projection
 // coverage across TP sizes", section "Scope": FP16 inputs with FP32
 // accumulation for both QK and PV).  For E4M3, K' and V' are the codes decoded
-// exactly to FP16 * 2^-8; for BF16, K' is K and V' is V converted to FP16 so
+// exactly to FP16; for BF16, K' is K and V' is V converted to FP16 so
 // that P can stay FP16 in the PV product.  Each TMEM lane is one key, so the
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <cstddef>
 
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -50,15 +51,15 @@ struct Fp8Fmt {
   static constexpr int kElemBytes = 1;
   static constexpr int kQBf16 = 0;                 // Q (and K') type of the QK product
   static __device__ __forceinline__ float score_scale(const float* k_scale) {
-    // S' = 2^-8 * q.k_code;  s * log2(e) = S' * 2^8 * k_scale / sqrt(256) * log2(e)
-    return __ldg(k_scale) * (kE4m3Unscale / 16.0f) * 1.4426950408889634f;
+    // S' = q . k_code;  s * log2(e) = S' * k_scale / sqrt(256) * log2(e)
+    return __ldg(k_scale) * (1.0f / 16.0f) * 1.4426950408889634f;
   }
   // 16 stored bytes (16 elements) -> 8 words of FP16x2 (K' or V' values)
   static __device__ __forceinline__ void decode16(uint4 x, uint32_t* w) {
-    e4m3x4_to_f16x4_scaled(x.x, w[0], w[1]);
-    e4m3x4_to_f16x4_scaled(x.y, w[2], w[3]);
-    e4m3x4_to_f16x4_scaled(x.z, w[4], w[5]);
-    e4m3x4_to_f16x4_scaled(x.w, w[6], w[7]);
+    e4m3x4_to_f16x4(x.x, w[0], w[1]);
+    e4m3x4_to_f16x4(x.y, w[2], w[3]);
+    e4m3x4_to_f16x4(x.z, w[4], w[5]);
+    e4m3x4_to_f16x4(x.w, w[6], w[7]);
   }
 };
 
@@ -104,11 +105,12 @@ struct Misc {
   WaitCtl ctl;
   int exceed_tag[2][4];
   int rescale_tag;
-  float mref[kMaxRows];
-  float alpha[kMaxRows];
-  float red[4][kMaxRows];
+  alignas(16) float mref[kMaxRows];  // read as float4
+  alignas(16) float alpha[kMaxRows];
+  alignas(16) float red[4][kMaxRows];
   Sched sched;
 };
+static_assert(offsetof(Misc, mref) % 16 == 0, "mref is read with 16-byte loads");
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;
 
 // Cross-lane reduction of n per-lane values (one per packed row) in a warp.
