@@ -163,6 +163,35 @@ int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const 
                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
                   const float* v_scale, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- FP16 Q x E4M3 K/V without a caller workspace ---------------------------
+ * Same operation, arguments and results as pa_decode_fp8, for callers that
+ * cannot allocate device memory: code running under another framework's
+ * memory manager, which gives a library no allocator of its own and would
+ * see a raw cudaMalloc bypass its pool (and cudaMalloc/cudaFree may
+ * synchronise the whole device), or a latency-critical host thread that must
+ * not block in the allocator.  The pages describe no such entry point; it is
+ * an addition of this library.
+ *
+ * Scratch memory: a PA_NOALLOC_SCRATCH_BYTES (16 MiB) array in device global
+ * memory, declared in the library, which every GPU that loads the library
+ * holds until the process exits.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).  Geometries whose workspace
+ * (pa_decode_fp8_workspace_bytes) exceeds the array are rejected with
+ * PA_ERR_WORKSPACE before anything is enqueued (B8 x 131072 keys, GQA 6,
+ * q_len 8 needs 12.7 MB and fits).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one array, which keeps the last call's contents; each call
+ * clears the parts that must start at zero (status word, per-request flags).
+ * Calls that overlap on the GPU (different streams, or several host threads)
+ * race on the array and give undefined results: serialise them.  The status
+ * word is cleared at the start of every call and cannot be read back.
+ * Returns PA_OK after enqueueing, or a negative pa_status. */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                          const float* v_scale, void* out, void* stream);
+
 /* ---- BF16 Q/K/V, head_dim 128 ----------------------------------------------
  *
  * The head-dim-128 BF16 decode with group packing ("perf(fa2): port decode GQA

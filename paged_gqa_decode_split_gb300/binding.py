@@ -21,6 +21,7 @@ PA_ERR_CUDA = -6
 PA_FLAG_BAD_PAGE = 0x1
 PA_FLAG_BAD_LENGTH = 0x2
 PA_FLAG_TIMEOUT = 0x4
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class pa_caps(ctypes.Structure):
@@ -65,6 +66,7 @@ def load() -> ctypes.CDLL:
             "pa_split_plan": ([i32, _P(i32), _P(i32)], ctypes.c_int),
             "pa_decode_fp8_workspace_bytes": ([pp], sz),
             "pa_decode_fp8": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "pa_decode_fp8_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "pa_decode_bf16_d128_workspace_bytes": ([pp], sz),
             "pa_decode_bf16_d128": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_read_status": ([vp, _P(ctypes.c_uint32), vp], ctypes.c_int),
@@ -155,6 +157,12 @@ def pa_decode_fp8(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, k_sc
     return load().pa_decode_fp8(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                 _ptr(ctx_lens), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(workspace),
                                 int(workspace_bytes), _stream(stream))
+
+
+def pa_decode_fp8_noalloc(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out,
+                          stream=None) -> int:
+    return load().pa_decode_fp8_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                        _ptr(ctx_lens), _ptr(k_scale), _ptr(v_scale), _ptr(out), _stream(stream))
 
 
 def pa_decode_bf16_d128(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, out, lse, workspace,

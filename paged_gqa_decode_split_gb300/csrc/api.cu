@@ -112,7 +112,8 @@ void timing_slot(int kind, cudaEvent_t* a, cudaEvent_t* b) {
 
 int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
-                  void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr) {
+                  void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr,
+                  bool clear_status = false) {
   const int D = bf16 ? 128 : 256;
   int R = 0;
   int st = check_geometry(p, D, &R);
@@ -137,6 +138,7 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* bad = reinterpret_cast<uint32_t*>(ws + kWsBadOff);
   if (cudaMemsetAsync(bad, 0, sizeof(uint32_t) * p->batch, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (clear_status && cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return PA_ERR_CUDA;
 
   SplitArgs a;
   a.q = q;
@@ -181,6 +183,28 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   if (e0) cudaEventRecord(e0, stream);
   if (launch_combine(c, bf16, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (e1) cudaEventRecord(e1, stream);
+  return PA_OK;
+}
+
+// ---- allocation-free variant ------------------------------------------------
+// Scratch for pa_decode_fp8_noalloc: a module-scope device array that every
+// device loading this library holds until the process exits.  Host code must
+// not use its name as an address; the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+constexpr size_t kNoallocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+int noalloc_scratch(int dev, void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {nullptr};
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
   return PA_OK;
 }
 
@@ -234,6 +258,22 @@ int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const 
                   void* out, void* workspace, size_t workspace_bytes_given, void* stream) {
   return decode_common(false, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
                        workspace, workspace_bytes_given, stream);
+}
+
+int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                          const float* v_scale, void* out, void* stream) {
+  int R = 0;
+  const int st = check_geometry(p, 256, &R);
+  if (st != PA_OK) return st;
+  if (workspace_bytes(p, 256) > kNoallocScratchBytes) return PA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  void* scratch = nullptr;
+  const int sst = noalloc_scratch(dev, &scratch);
+  if (sst != PA_OK) return sst;
+  return decode_common(false, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
+                       scratch, kNoallocScratchBytes, stream, /*clear_status=*/true);
 }
 
 int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
