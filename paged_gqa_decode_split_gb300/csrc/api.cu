@@ -1,6 +1,8 @@
 // C ABI of libpa (declared in include/pa.h): host-side validation, workspace
 // layout, launches and the timing / bookkeeping helpers.  No device memory is
 // allocated here; every buffer belongs to the caller.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -74,6 +76,41 @@ bool strides16(const pa_params* p, const void* k, const void* v) {
          p->v_head_stride % 16 == 0;
 }
 
+// ---- TMA tensor maps ----------------------------------------------------------
+// The driver's tensor-map encoder, fetched through the runtime so the library
+// does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D byte view of K or V: (row byte 0..255, KV head, slot, page), boxes of
+// 128 bytes x 1 head x 16 slots, 128-byte swizzle.
+bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const long long hs = v ? p->v_head_stride : p->k_head_stride;
+  const long long ts = v ? p->v_token_stride : p->k_token_stride;
+  const long long ps = v ? p->v_page_stride : p->k_page_stride;
+  cuuint64_t dims[4] = {256, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size, (cuuint64_t)p->num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)(p->num_kv_heads == 1 ? 256 : hs), (cuuint64_t)ts, (cuuint64_t)ps};
+  cuuint32_t box[4] = {128, 1, 16, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (cuuint64_t s : strides)
+    if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- kernel timing ----------------------------------------------------------
 struct Timing {
   std::mutex mu;
@@ -141,6 +178,7 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   if (clear_status && cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return PA_ERR_CUDA;
 
   SplitArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.q = q;
   a.k = static_cast<const uint8_t*>(k_pages);
   a.v = static_cast<const uint8_t*>(v_pages);
@@ -156,6 +194,9 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;
   a.q_len = p->q_len, a.R = R, a.page_size = p->page_size, a.mpr = p->max_pages_per_req;
   a.num_pages = p->num_pages, a.max_ctx = p->max_ctx_len, a.s_max = s_max;
+  // TMA loads need 16-byte aligned bases and strides; 8-byte aligned data uses cp.async
+  a.use_tma = strides16(p, k_pages, v_pages) && encode_kv_map(&a.k_map, k_pages, p, false) &&
+              encode_kv_map(&a.v_map, v_pages, p, true);
   const long long stall = g_stall_next.exchange(0);
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;
@@ -165,7 +206,7 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   cudaEvent_t e0, e1;
   timing_slot(0, &e0, &e1);
   if (e0) cudaEventRecord(e0, stream);
-  if (launch_split(a, bf16, grid, strides16(p, k_pages, v_pages), stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_split(a, bf16, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (e1) cudaEventRecord(e1, stream);
 
   CombineArgs c;

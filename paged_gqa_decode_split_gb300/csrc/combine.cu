@@ -17,8 +17,12 @@ namespace pa {
 
 namespace {
 
+static_assert(kMaxSplits <= 32, "one warp computes the split weights");
+
 template <bool BF16OUT>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float lsum_s;
   const int row = blockIdx.x % a.R;
   const int bg = blockIdx.x / a.R;
   const int g = bg % a.Hkv;
@@ -28,30 +32,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   if (L < 0 || L > a.max_ctx) L = 0;
   int ns, chunk;
   split_plan(L, ns, chunk);
-  const bool bad = a.bad != nullptr && a.bad[b] != 0u;
+  if (a.bad != nullptr && a.bad[b] != 0u) ns = 0;
   const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
   const size_t prow = (size_t)bg * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
-  float M = -INFINITY;
-  if (!bad)
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.panel_ml[prow + (size_t)s * a.R].x);
-  float lsum = 0.f;
-  if (M != -INFINITY)
-    for (int s = 0; s < ns; ++s) {
+  // one warp: M = max_s m_s, w_s = 2^(m_s - M), lsum = sum_s w_s l_s
+  if (threadIdx.x < 32) {
+    const int s = threadIdx.x;
+    float m = -INFINITY, l = 0.f;
+    if (s < ns) {
       const float2 ml = a.panel_ml[prow + (size_t)s * a.R];
-      const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-      lsum += w * ml.y;
+      m = ml.x;
+      l = ml.y;
     }
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+    float ls = w * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (s < kMaxSplits) w_s[s] = w;
+    if (s == 0) {
+      lsum_s = ls;
+      if (a.lse != nullptr)
+        a.lse[orow] = (M == -INFINITY || !(ls > 0.f)) ? -INFINITY : (M + log2f(ls)) * 0.6931471805599453f;
+    }
+  }
+  __syncthreads();
+  const float lsum = lsum_s;
   const float scale = (a.out_scale_ptr ? __ldg(a.out_scale_ptr) : 1.0f) * a.out_scale_mul;
+  const float* o0 = a.panel_o + prow * a.D;
+  const size_t sstride = (size_t)a.R * a.D;
   for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
     float val = 0.f;
-    if (M != -INFINITY && lsum > 0.f) {
+    if (lsum > 0.f) {
+      // all loads issued up front; accumulation in ascending split order
+      float o[kMaxSplits];
+#pragma unroll
+      for (int s = 0; s < kMaxSplits; ++s) o[s] = (s < ns) ? __ldg(o0 + s * sstride + d) : 0.f;
       float acc = 0.f;
-      for (int s = 0; s < ns; ++s) {
-        const size_t pr = prow + (size_t)s * a.R;
-        const float2 ml = a.panel_ml[pr];
-        const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-        acc += w * a.panel_o[pr * a.D + d];
-      }
+#pragma unroll
+      for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(w_s[s], o[s], acc) : acc;
       val = acc / lsum * scale;
     }
     if constexpr (BF16OUT) {
@@ -59,9 +80,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     } else {
       reinterpret_cast<__half*>(a.out)[orow * a.D + d] = __float2half_rn(val);
     }
-  }
-  if (a.lse != nullptr && threadIdx.x == 0) {
-    a.lse[orow] = (M == -INFINITY || !(lsum > 0.f)) ? -INFINITY : (M + log2f(lsum)) * 0.6931471805599453f;
   }
 }
 

@@ -2,12 +2,18 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pa {
 
 // Split-KV kernel arguments (both element formats).
 struct SplitArgs {
+  // 4-D byte views (row byte, KV head, slot, page) of K and V for the TMA
+  // loaders; filled when use_tma != 0 (16-byte aligned bases and strides)
+  CUtensorMap k_map;
+  CUtensorMap v_map;
+  int use_tma;
   const void* q;               // FP16 (E4M3 path) or BF16 (BF16 path) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs
   const uint8_t* v;
@@ -37,7 +43,7 @@ struct CombineArgs {
 };
 
 int split_smem_bytes();
-cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, bool vec16, cudaStream_t stream);
+cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream);
 cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
                                   int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream);

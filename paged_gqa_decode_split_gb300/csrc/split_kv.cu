@@ -21,8 +21,8 @@
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
 // Warp roles (16 warps):
-//   0  K loader   cp.async of K rows, gathered through the block table, into a
-//                 32-key staging ring (zero-filled past the split end)
+//   0  K loader   TMA (or cp.async for 8-byte aligned data) of block-table-
+//                 gathered K rows into a 32-key staging ring
 //   2  V loader   the same for V
 //   3  Q loader   the packed Q tile of each item (128-byte swizzle)
 //   1  MMA        one thread issues tcgen05.mma and commits to mbarriers
@@ -81,7 +81,9 @@ struct Bf16Fmt {
 
 constexpr int kStages = 4;         // staging ring depth per tensor, in 32-key chunks
 constexpr int kChunkKeys = 32;
+constexpr int kPageSeg = 8;       // chunks whose page ids a loader lane holds in registers
 constexpr float kTau = 8.0f;       // a row's reference max moves only when a score exceeds it by 2^8
+constexpr float kNoMax = -1e30f;   // reference max of a row that has seen no key (finite: 2^(s - kNoMax) never NaN)
 constexpr int kThreads = 512;
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -106,6 +108,7 @@ struct Misc {
   int exceed_tag[2][4];
   int rescale_tag;
   alignas(16) float mref[kMaxRows];  // read as float4
+  alignas(16) float thr[kMaxRows];   // (mref + tau) / c: scores above this need a new reference
   alignas(16) float alpha[kMaxRows];
   alignas(16) float red[4][kMaxRows];
   Sched sched;
@@ -197,16 +200,34 @@ __device__ __forceinline__ int tiles_of(const Item& x) { return (x.t1 - x.t0 + k
 
 // ------------------------------------------------------------------ roles --
 
+// Key row kk of a stage (see role_loader) as 16 pieces of 16 bytes; zeros
+// for keys past the split end (their stage bytes are stale or a page tail).
+__device__ __forceinline__ void load_stage_row(const uint8_t* stage, int kk, bool live, uint4 (&raw)[16]) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    raw[p] = live ? *reinterpret_cast<const uint4*>(stage + (p >> 3) * 4096 + kk * 128 + (((p & 7) ^ (kk & 7)) << 4))
+                  : make_uint4(0u, 0u, 0u, 0u);
+}
+
 // K or V loader: 32-key chunks into the staging ring.  Chunk c of the CTA's
-// item sequence goes to stage c % kStages.  Row kk of a stage (256 bytes) is at
-// kk*256 and its 16-byte piece ch at ((ch ^ (kk & 7)) * 16), so the decode
-// warps read eight consecutive keys without bank conflicts.
-template <int VEC>
+// item sequence goes to stage c % kStages.  Stage layout: two halves of the
+// 256-byte key rows, half h at h*4096, key kk's 128 bytes at kk*128 with its
+// 16-byte piece p at ((p ^ (kk & 7)) * 16) (the TMA 128-byte swizzle), so the
+// decode warps read eight consecutive keys without bank conflicts.
+//
+// TMA mode (16-byte aligned bases and strides): one thread issues, per 16-key
+// block, two 2 KB boxes (row bytes 0-127 and 128-255) of the 4-D byte view
+// (row byte, KV head, slot, page); completion is counted in bytes on the
+// stage's full barrier.  Blocks entirely past the split end are not loaded.
+// cp.async mode (8-byte aligned data): every lane copies 8-byte pieces of the
+// chunk's rows into the same layout, zero-filling rows past the split end.
+template <int USE_TMA>
 __device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is_v, int lane) {
   const uint8_t* base = is_v ? a.v : a.k;
   const long long pstr = is_v ? a.v_ps : a.k_ps;
   const long long tstr = is_v ? a.v_ts : a.k_ts;
   const long long hstr = is_v ? a.v_hs : a.k_hs;
+  const CUtensorMap* map = is_v ? &a.v_map : &a.k_map;
   uint64_t* full = is_v ? M.vst_full : M.kst_full;
   uint64_t* empty = is_v ? M.vst_empty : M.kst_empty;
   uint8_t* ring = smem_base() + (is_v ? kOffVst : kOffKst);
@@ -217,45 +238,86 @@ __device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is
     const int32_t* bt = a.block_table + (size_t)x.b * a.mpr;
     const uint8_t* hbase = base + (long long)x.g * hstr;
     const int nchunks = tiles_of(x) * (kTileKeys / kChunkKeys);
-    for (int ci = 0; ci < nchunks; ++ci, ++c) {
-      const int st = c % kStages;
-      const uint32_t ph = (c / kStages) & 1;
-      if (!mbar_wait(&empty[st], ph ^ 1, abort)) goto done;
-      const int kb = x.t0 + ci * kChunkKeys;
-      // lane l resolves the row of key kb + l once; the others read it by shuffle
-      const int tk = kb + lane;
-      long long rowoff = -1;
-      if (tk < x.t1) {
-        rowoff = kv_row_offset(bt, tk, a.page_size, a.num_pages, pstr, tstr);
-        if (rowoff < 0) {
-          atomicOr(a.status, 0x1u);
-          atomicOr(a.bad + x.b, 1u);
-        }
+    // Page id of key t0 + 32*cj + lane, for 8 chunks at a time in registers:
+    // `cur` serves chunks cs..cs+7 while `nxt` is being loaded for cs+8..cs+15,
+    // so the block-table latency (long under full HBM load) stays hidden.
+    auto load_segment = [&](int (&pg)[kPageSeg], int cs) {
+#pragma unroll
+      for (int s = 0; s < kPageSeg; ++s) {
+        const int cj = cs + s;
+        const int t = x.t0 + cj * kChunkKeys + lane;
+        pg[s] = (cj < nchunks && t < x.t1) ? __ldg(bt + t / a.page_size) : -1;
       }
-      const uint32_t dst0 = smem_u32(ring + st * (kChunkKeys * 256));
-      if constexpr (VEC == 16) {
+    };
+    int cur[kPageSeg], nxt[kPageSeg];
+    load_segment(cur, 0);
+    load_segment(nxt, kPageSeg);
+    for (int cs = 0; cs < nchunks; cs += kPageSeg) {
+#pragma unroll
+      for (int s = 0; s < kPageSeg; ++s) {
+        const int ci = cs + s;
+        if (ci >= nchunks) break;
+        const int st = c % kStages;
+        const uint32_t ph = (c / kStages) & 1;
+        const int page_cur = cur[s];
+        if (!mbar_wait(&empty[st], ph ^ 1, abort)) goto done;
+        const int kb = x.t0 + ci * kChunkKeys;
+        const uint32_t dst0 = smem_u32(ring + st * (kChunkKeys * 256));
+        if constexpr (USE_TMA) {
+          // lanes 0 and 16 hold the pages of the chunk's two 16-key blocks
+          const int t = kb + lane;
+          bool ok = (lane & 15) == 0 && t < x.t1;
+          if (ok && (unsigned)page_cur >= (unsigned)a.num_pages) {
+            atomicOr(a.status, 0x1u);
+            atomicOr(a.bad + x.b, 1u);
+            ok = false;
+          }
+          const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+          const int pg0 = __shfl_sync(0xffffffffu, page_cur, 0), pg1 = __shfl_sync(0xffffffffu, page_cur, 16);
+          if (lane == 0) {
+            const uint32_t blocks = (okmask & 1u) + ((okmask >> 16) & 1u);
+            mbar_arrive_expect_tx(&full[st], 4096u * blocks);
+#pragma unroll
+            for (int sb = 0; sb < 2; ++sb) {
+              if (!(okmask >> (16 * sb) & 1u)) continue;
+              const int pg = sb ? pg1 : pg0;
+              const int slot = (kb + 16 * sb) % a.page_size;
+              tma_load_4d(dst0 + sb * 2048, map, 0, x.g, slot, pg, &full[st]);
+              tma_load_4d(dst0 + 4096 + sb * 2048, map, 128, x.g, slot, pg, &full[st]);
+            }
+          }
+          __syncwarp();
+        } else {
+          const int t = kb + lane;
+          long long rowoff = -1;
+          if (t < x.t1) {
+            if ((unsigned)page_cur < (unsigned)a.num_pages) {
+              rowoff = (long long)page_cur * pstr + (long long)(t % a.page_size) * tstr;
+            } else {
+              atomicOr(a.status, 0x1u);
+              atomicOr(a.bad + x.b, 1u);
+            }
+          }
 #pragma unroll 4
-        for (int s2 = 0; s2 < kChunkKeys / 2; ++s2) {
-          const int kk = 2 * s2 + (lane >> 4);
-          const int ch = lane & 15;
-          const long long ro = __shfl_sync(0xffffffffu, rowoff, kk);
-          const uint8_t* src = ro >= 0 ? hbase + ro + ch * 16 : base;
-          cp_async_16(dst0 + kk * 256 + ((ch ^ (kk & 7)) << 4), src, ro >= 0 ? 16u : 0u);
+          for (int kk = 0; kk < kChunkKeys; ++kk) {
+            const long long ro = __shfl_sync(0xffffffffu, rowoff, kk);
+            const int piece = lane >> 1;  // 16-byte piece 0..15 of the row
+            const uint8_t* src = ro >= 0 ? hbase + ro + lane * 8 : base;
+            const uint32_t dst =
+                dst0 + (piece >> 3) * 4096 + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4) + (lane & 1) * 8;
+            cp_async_8(dst, src, ro >= 0 ? 8u : 0u);
+          }
+          cp_async_arrive(&full[st]);
         }
-      } else {
-#pragma unroll 4
-        for (int kk = 0; kk < kChunkKeys; ++kk) {
-          const int ch = lane >> 1;
-          const long long ro = __shfl_sync(0xffffffffu, rowoff, kk);
-          const uint8_t* src = ro >= 0 ? hbase + ro + lane * 8 : base;
-          cp_async_8(dst0 + kk * 256 + ((ch ^ (kk & 7)) << 4) + (lane & 1) * 8, src, ro >= 0 ? 8u : 0u);
-        }
+        ++c;
       }
-      cp_async_arrive(&full[st]);
+#pragma unroll
+      for (int s = 0; s < kPageSeg; ++s) cur[s] = nxt[s];
+      load_segment(nxt, cs + 2 * kPageSeg);
     }
   }
 done:
-  cp_async_wait_all();
+  if constexpr (!USE_TMA) cp_async_wait_all();
 }
 
 // Q loader: packed row r = qi * G + hl holds query head g*G + hl of verify
@@ -302,18 +364,19 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
       const uint32_t c = 4 * j + i;
       const int st = c % kStages;
       if (!mbar_wait(&M.kst_full[st], (c / kStages) & 1, abort)) return;
+      // take this key's 256-byte row into registers and hand the stage back
+      // at once, so the loader's refill does not wait for the tensor core
+      uint4 raw[16];
+      load_stage_row(ring + st * (kChunkKeys * 256), lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
+      mbar_arrive(&M.kst_empty[st]);
       if (!mbar_wait(&M.kbuf_empty[j & 1], ((j >> 1) & 1) ^ 1, abort)) return;
-      const uint8_t* row = ring + st * (kChunkKeys * 256) + lane * 256;
       const uint32_t taddr = tb + ((uint32_t)(32 * i) << 16) + kColK + (j & 1) * 128;
       if constexpr (Fmt::kElemBytes == 1) {
 #pragma unroll
         for (int c2 = 0; c2 < 8; ++c2) {
           uint32_t r[16];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int ch = 2 * c2 + h;
-            Fmt::decode16(*reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) << 4)), r + 8 * h);
-          }
+          Fmt::decode16(raw[2 * c2], r);
+          Fmt::decode16(raw[2 * c2 + 1], r + 8);
           PA_TMEM_ST_X16(taddr + c2 * 16, r);
         }
       } else {
@@ -322,8 +385,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
           uint32_t r[16];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const int ch = 4 * c4 + h;
-            const uint4 w = *reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) << 4));
+            const uint4 w = raw[4 * c4 + h];
             r[4 * h + 0] = w.x, r[4 * h + 1] = w.y, r[4 * h + 2] = w.z, r[4 * h + 3] = w.w;
           }
           PA_TMEM_ST_X16(taddr + c4 * 16, r);
@@ -332,10 +394,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&M.kst_empty[st]);
-        mbar_arrive(&M.kbuf_full[j & 1]);
-      }
+      if (lane == 0) mbar_arrive(&M.kbuf_full[j & 1]);
     }
   }
 }
@@ -357,11 +416,14 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
       const uint32_t c = 4 * j + i;
       const int st = c % kStages;
       if (!mbar_wait(&M.vst_full[st], (c / kStages) & 1, abort)) return;
+      // row into registers, stage back to the loader, then wait for PV(j-1)
+      uint4 raw[16];
+      load_stage_row(ring + st * (kChunkKeys * 256), lane, x.t0 + jl * kTileKeys + key < x.t1, raw);
+      mbar_arrive(&M.vst_empty[st]);
       if (j > 0 && !mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
-      const uint8_t* row = ring + st * (kChunkKeys * 256) + lane * 256;
-#pragma unroll 4
+#pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
-        const uint4 x4 = *reinterpret_cast<const uint4*>(row + ((ch ^ (lane & 7)) << 4));
+        const uint4 x4 = raw[ch];
         if constexpr (Fmt::kElemBytes == 1) {
           // piece ch = d 16ch .. 16ch+15 -> two 8-element FP16 pieces
           uint32_t w[8];
@@ -380,10 +442,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&M.vst_empty[st]);
-        mbar_arrive(&M.vbuf_full);
-      }
+      if (lane == 0) mbar_arrive(&M.vbuf_full);
     }
   }
 }
@@ -449,6 +508,14 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
 }
 
 // Softmax warps: quarter i reads TMEM lanes 32i.. (keys of S^T, then d of O^T).
+//
+// Scores stay in S units (the raw QK^T accumulator); c = log2(e) * scale turns
+// them into the log2 domain inside one FFMA.  Per row r the group keeps a
+// reference max m_r (log2 units; kNoMax before any visible key) and the
+// threshold thr_r = (m_r + tau) / c: a tile needs a new reference only if some
+// visible score exceeds thr_r, so the common tile is P = 2^(S*c - m_r) with no
+// cross-lane reduction.  Each thread keeps the running row sums of its own key
+// slot for all rows and the group reduces them once per item.
 template <class Fmt, int NM>
 __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb) {
   using BF = Butterfly<NM, 16>;
@@ -472,64 +539,76 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
     const int lim = x.L - a.q_len;  // packed row r sees key t iff t <= lim + r / G
-    float lacc[CNT];
+    float lsum[NM];                 // running row sums of this thread's key slot
 #pragma unroll
-    for (int k = 0; k < CNT; ++k) lacc[k] = 0.f;
+    for (int r = 0; r < NM; ++r) lsum[r] = 0.f;
     for (int jl = 0; jl < nt; ++jl, ++j) {
       if (!mbar_wait(&M.s_full[j & 1], (j >> 1) & 1, abort)) return;
       tc_fence_after();
-      float t[NM];
-#pragma unroll
-      for (int c16 = 0; c16 < NM / 16; ++c16) {
-        uint32_t r[16];
-        tmem_load16(lane_base + kColS + (j & 1) * 64 + 16 * c16, r);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) t[16 * c16 + k] = __uint_as_float(r[k]) * c_log2;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&M.s_empty[j & 1]);
-
+      const uint32_t s_addr = lane_base + kColS + (j & 1) * 64;
       const int tile0 = x.t0 + jl * kTileKeys;
       const int key = tile0 + gt;
       const int vis_end = min(x.t1, lim + 1);  // keys below this are visible to every row
-      if (tile0 + kTileKeys > vis_end || NM > a.R) {
+      const bool masked_tile = tile0 + kTileKeys > vis_end || NM > a.R;
+      // 16 scores of columns 16*c16.. from TMEM, masked to -inf where invisible
+      auto load_chunk = [&](int c16, float (&v)[16]) {
+        uint32_t r[16];
+        tmem_load16(s_addr + 16 * c16, r);
 #pragma unroll
-        for (int r = 0; r < NM; ++r) {
-          const bool vis = (r < a.R) && (key < x.t1) && (key <= lim + r / a.G);
-          if (!vis) t[r] = -INFINITY;
+        for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+        if (masked_tile) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int row = 16 * c16 + k;
+            const bool vis = (row < a.R) && (key < x.t1) && (key <= lim + row / a.G);
+            if (!vis) v[k] = -INFINITY;
+          }
         }
-      }
-      // lazy max: only a score above its row's reference max + tau forces an update
+      };
+      // pass 1: does any visible score exceed its row's threshold?
       bool ex = false;
 #pragma unroll
-      for (int r = 0; r < NM; r += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(&M.mref[r]);
-        ex |= (t[r] > m4.x + kTau) | (t[r + 1] > m4.y + kTau) | (t[r + 2] > m4.z + kTau) | (t[r + 3] > m4.w + kTau);
+      for (int c16 = 0; c16 < NM / 16; ++c16) {
+        float v[16];
+        load_chunk(c16, v);
+#pragma unroll
+        for (int k = 0; k < 16; k += 4) {
+          const float4 th = *reinterpret_cast<const float4*>(&M.thr[16 * c16 + k]);
+          ex |= (v[k] > th.x) | (v[k + 1] > th.y) | (v[k + 2] > th.z) | (v[k + 3] > th.w);
+        }
       }
       if (__any_sync(0xffffffffu, ex) && lane == 0) M.exceed_tag[j & 1][i] = (int)j + 1;
       if (!group_sync()) return;
       const int* tag = M.exceed_tag[j & 1];
       const bool slow = tag[0] == (int)j + 1 || tag[1] == (int)j + 1 || tag[2] == (int)j + 1 || tag[3] == (int)j + 1;
       if (slow) {
-        float mx[BF::Half];
-        BF::template run_from<true>(t, mx, lane);
+        // tile max per row: a 16-row butterfly per chunk leaves one row per lane
+        using BF16 = Butterfly<16, 16>;
 #pragma unroll
-        for (int k = 0; k < CNT; ++k) M.red[i][rbase + k] = mx[k];
+        for (int c16 = 0; c16 < NM / 16; ++c16) {
+          float v[16], mx[BF16::Half];
+          load_chunk(c16, v);
+          BF16::template run_from<true>(v, mx, lane);
+          M.red[i][16 * c16 + BF16::base(lane)] = mx[0];
+        }
         if (!group_sync()) return;
         if (gt < NM) {
           const float m_old = M.mref[gt];
-          const float tm = fmaxf(fmaxf(M.red[0][gt], M.red[1][gt]), fmaxf(M.red[2][gt], M.red[3][gt]));
-          const float m_new = fmaxf(m_old, tm);
+          const float tmax = fmaxf(fmaxf(M.red[0][gt], M.red[1][gt]), fmaxf(M.red[2][gt], M.red[3][gt]));
+          const float m_new = fmaxf(m_old, tmax * c_log2);  // tmax = -inf keeps m_old
           const float al = (m_new == m_old) ? 1.0f : exp2f(m_old - m_new);
           M.mref[gt] = m_new;
+          M.thr[gt] = (m_new + kTau) / c_log2;
           M.alpha[gt] = al;
           if (al != 1.0f) M.rescale_tag = (int)j + 1;
         }
         if (!group_sync()) return;
         if (M.rescale_tag == (int)j + 1) {
 #pragma unroll
-          for (int k = 0; k < CNT; ++k) lacc[k] *= M.alpha[rbase + k];
+          for (int r = 0; r < NM; r += 4) {
+            const float4 al = *reinterpret_cast<const float4*>(&M.alpha[r]);
+            lsum[r] *= al.x, lsum[r + 1] *= al.y, lsum[r + 2] *= al.z, lsum[r + 3] *= al.w;
+          }
           if (jl > 0) {
             // O^T holds tiles < j: wait for PV(j-1), then scale column r by alpha[r]
             if (!mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
@@ -550,48 +629,61 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
           }
         }
       }
-      // probabilities -> P^T row of this key (MN-major: one 128-byte row per
-      // key, 8-row pieces swizzled); P[j&1] is free once PV(j-2) completed
+      // pass 2: probabilities -> P^T row of this key (MN-major: one 128-byte
+      // row per key, 8-row pieces swizzled); P[j&1] is free once PV(j-2) is
+      // done.  A masked score is -inf, so its probability is exactly 0.
       if (j >= 2 && !mbar_wait(&M.pv_done[j & 1], ((j - 2) >> 1) & 1, abort)) return;
-      float* p = t;  // probabilities overwrite the scores
-#pragma unroll
-      for (int r = 0; r < NM; r += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(&M.mref[r]);
-        p[r] = (t[r] == -INFINITY) ? 0.f : ex2_approx(t[r] - m4.x);
-        p[r + 1] = (t[r + 1] == -INFINITY) ? 0.f : ex2_approx(t[r + 1] - m4.y);
-        p[r + 2] = (t[r + 2] == -INFINITY) ? 0.f : ex2_approx(t[r + 2] - m4.z);
-        p[r + 3] = (t[r + 3] == -INFINITY) ? 0.f : ex2_approx(t[r + 3] - m4.w);
-      }
       uint8_t* prow = pbuf + (j & 1) * 16384 + gt * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < NM / 8; ++c8) {
-        __half2 h0 = __floats2half2_rn(p[8 * c8 + 0], p[8 * c8 + 1]);
-        __half2 h1 = __floats2half2_rn(p[8 * c8 + 2], p[8 * c8 + 3]);
-        __half2 h2 = __floats2half2_rn(p[8 * c8 + 4], p[8 * c8 + 5]);
-        __half2 h3 = __floats2half2_rn(p[8 * c8 + 6], p[8 * c8 + 7]);
-        uint4 w;
-        w.x = *reinterpret_cast<uint32_t*>(&h0);
-        w.y = *reinterpret_cast<uint32_t*>(&h1);
-        w.z = *reinterpret_cast<uint32_t*>(&h2);
-        w.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (gt & 7)) << 4)) = w;
-      }
-      BF::template run<false>(p, lane);
+      for (int c16 = 0; c16 < NM / 16; ++c16) {
+        float v[16];
+        load_chunk(c16, v);
 #pragma unroll
-      for (int k = 0; k < CNT; ++k) lacc[k] += p[k];
-      fence_proxy_async_smem();
+        for (int h8 = 0; h8 < 2; ++h8) {
+          const int c8 = 2 * c16 + h8;
+          const float4 m0 = *reinterpret_cast<const float4*>(&M.mref[8 * c8]);
+          const float4 m1 = *reinterpret_cast<const float4*>(&M.mref[8 * c8 + 4]);
+          const float* u = v + 8 * h8;
+          float p[8];
+          p[0] = ex2_approx(fmaf(u[0], c_log2, -m0.x));
+          p[1] = ex2_approx(fmaf(u[1], c_log2, -m0.y));
+          p[2] = ex2_approx(fmaf(u[2], c_log2, -m0.z));
+          p[3] = ex2_approx(fmaf(u[3], c_log2, -m0.w));
+          p[4] = ex2_approx(fmaf(u[4], c_log2, -m1.x));
+          p[5] = ex2_approx(fmaf(u[5], c_log2, -m1.y));
+          p[6] = ex2_approx(fmaf(u[6], c_log2, -m1.z));
+          p[7] = ex2_approx(fmaf(u[7], c_log2, -m1.w));
+          __half2 h0 = __floats2half2_rn(p[0], p[1]);
+          __half2 h1 = __floats2half2_rn(p[2], p[3]);
+          __half2 h2 = __floats2half2_rn(p[4], p[5]);
+          __half2 h3 = __floats2half2_rn(p[6], p[7]);
+          uint4 w;
+          w.x = *reinterpret_cast<uint32_t*>(&h0);
+          w.y = *reinterpret_cast<uint32_t*>(&h1);
+          w.z = *reinterpret_cast<uint32_t*>(&h2);
+          w.w = *reinterpret_cast<uint32_t*>(&h3);
+          *reinterpret_cast<uint4*>(prow + ((c8 ^ (gt & 7)) << 4)) = w;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) lsum[8 * c8 + k] += p[k];
+        }
+      }
+      // S[j&1] may now be overwritten by QK(j+2)
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.s_empty[j & 1]);
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.p_full[j & 1]);
     }
     // ---- epilogue: (m, l, O) partials of this item
+    BF::template run<false>(lsum, lane);
 #pragma unroll
-    for (int k = 0; k < CNT; ++k) M.red[i][rbase + k] = lacc[k];
+    for (int k = 0; k < CNT; ++k) M.red[i][rbase + k] = lsum[k];
     if (!group_sync()) return;
     const size_t pi = panel_index(a, x);
     if (gt < a.R) {
       const float l = (M.red[0][gt] + M.red[1][gt]) + (M.red[2][gt] + M.red[3][gt]);
-      a.panel_ml[pi + gt] = make_float2(M.mref[gt], l);
+      a.panel_ml[pi + gt] = make_float2(l > 0.f ? M.mref[gt] : -INFINITY, l);
     }
     if (!mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
     tc_fence_after();
@@ -612,12 +704,15 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
     __syncwarp();
     if (lane == 0) mbar_arrive(&M.o_free);
     if (!group_sync()) return;
-    if (gt < kMaxRows) M.mref[gt] = -INFINITY;
+    if (gt < kMaxRows) {
+      M.mref[gt] = kNoMax;
+      M.thr[gt] = -INFINITY;
+    }
     if (!group_sync()) return;
   }
 }
 
-template <class Fmt, int NM, int VEC>
+template <class Fmt, int NM, int TMA>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitArgs a) {
   uint8_t* sm = smem_base();
   Misc& M = *reinterpret_cast<Misc*>(sm + kOffMisc);
@@ -625,10 +720,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&M.kst_full[s], 32);
-      mbar_init(&M.vst_full[s], 32);
-      mbar_init(&M.kst_empty[s], 1);
-      mbar_init(&M.vst_empty[s], 1);
+      mbar_init(&M.kst_full[s], a.use_tma ? 1 : 32);
+      mbar_init(&M.vst_full[s], a.use_tma ? 1 : 32);
+      mbar_init(&M.kst_empty[s], 32);
+      mbar_init(&M.vst_empty[s], 32);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&M.kbuf_full[s], 4);
@@ -650,7 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     for (int w = 0; w < 8; ++w) M.exceed_tag[w / 4][w % 4] = 0;
     mbar_fence_init();
   }
-  if (tid < kMaxRows) M.mref[tid] = -INFINITY;
+  if (tid < kMaxRows) {
+    M.mref[tid] = kNoMax;
+    M.thr[tid] = -INFINITY;
+  }
   if (warp == 1) tmem_alloc(&M.tmem_base, 512);
   // zero the Q tile (rows >= R stay zero) and both P^T buffers (rows >= N stay zero)
   for (int o = tid * 16; o < 32768; o += kThreads * 16) *reinterpret_cast<uint4*>(sm + kOffQ + o) = make_uint4(0, 0, 0, 0);
@@ -663,9 +761,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   const uint32_t tb = M.tmem_base;
 
   if (warp == 0) {
-    role_loader<VEC>(a, M, false, lane);
+    role_loader<TMA>(a, M, false, lane);
   } else if (warp == 2) {
-    role_loader<VEC>(a, M, true, lane);
+    role_loader<TMA>(a, M, true, lane);
   } else if (warp == 3) {
     role_qload<Fmt>(a, M, lane);
   } else if (warp == 1) {
@@ -695,9 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   if (tid == 0 && M.ctl.abort) atomicOr(a.status, 0x4u);
 }
 
-template <class Fmt, int NM, int VEC>
+template <class Fmt, int NM, int TMA>
 cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
-  auto kern = split_kernel<Fmt, NM, VEC>;
+  auto kern = split_kernel<Fmt, NM, TMA>;
   // the attribute is per device; setting it is idempotent, so a racing second
   // setter is harmless
   static std::atomic<uint64_t> set_on_devices{0};
@@ -714,13 +812,13 @@ cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <class Fmt, int VEC>
-cudaError_t launch_vec(const SplitArgs& a, int grid, cudaStream_t stream) {
+template <class Fmt, int TMA>
+cudaError_t launch_mode(const SplitArgs& a, int grid, cudaStream_t stream) {
   switch ((a.R + 15) / 16 * 16) {
-    case 16: return launch_one<Fmt, 16, VEC>(a, grid, stream);
-    case 32: return launch_one<Fmt, 32, VEC>(a, grid, stream);
-    case 48: return launch_one<Fmt, 48, VEC>(a, grid, stream);
-    case 64: return launch_one<Fmt, 64, VEC>(a, grid, stream);
+    case 16: return launch_one<Fmt, 16, TMA>(a, grid, stream);
+    case 32: return launch_one<Fmt, 32, TMA>(a, grid, stream);
+    case 48: return launch_one<Fmt, 48, TMA>(a, grid, stream);
+    case 64: return launch_one<Fmt, 64, TMA>(a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -729,9 +827,9 @@ cudaError_t launch_vec(const SplitArgs& a, int grid, cudaStream_t stream) {
 
 int split_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, bool vec16, cudaStream_t stream) {
-  if (bf16) return vec16 ? launch_vec<Bf16Fmt, 16>(a, grid, stream) : launch_vec<Bf16Fmt, 8>(a, grid, stream);
-  return vec16 ? launch_vec<Fp8Fmt, 16>(a, grid, stream) : launch_vec<Fp8Fmt, 8>(a, grid, stream);
+cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, cudaStream_t stream) {
+  if (bf16) return a.use_tma ? launch_mode<Bf16Fmt, 1>(a, grid, stream) : launch_mode<Bf16Fmt, 0>(a, grid, stream);
+  return a.use_tma ? launch_mode<Fp8Fmt, 1>(a, grid, stream) : launch_mode<Fp8Fmt, 0>(a, grid, stream);
 }
 
 }  // namespace pa
