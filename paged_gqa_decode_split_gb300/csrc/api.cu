@@ -93,8 +93,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 4-D byte view of K or V: (row byte 0..255, KV head, slot, page), boxes of
-// 128 bytes x 1 head x 16 slots, 128-byte swizzle.
-bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v) {
+// 128 bytes x 1 head x `slots` slots, 128-byte swizzle.  A box taller than a
+// page is clipped to the page (the loader never uses a box taller than the
+// piece of a page it copies).
+bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v, unsigned slots) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const long long hs = v ? p->v_head_stride : p->k_head_stride;
@@ -102,7 +104,7 @@ bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v)
   const long long ps = v ? p->v_page_stride : p->k_page_stride;
   cuuint64_t dims[4] = {256, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size, (cuuint64_t)p->num_pages};
   cuuint64_t strides[3] = {(cuuint64_t)(p->num_kv_heads == 1 ? 256 : hs), (cuuint64_t)ts, (cuuint64_t)ps};
-  cuuint32_t box[4] = {128, 1, 16, 1};
+  cuuint32_t box[4] = {128, 1, slots < (unsigned)p->page_size ? slots : (cuuint32_t)p->page_size, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   for (cuuint64_t s : strides)
     if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
@@ -195,8 +197,12 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   a.q_len = p->q_len, a.R = R, a.page_size = p->page_size, a.mpr = p->max_pages_per_req;
   a.num_pages = p->num_pages, a.max_ctx = p->max_ctx_len, a.s_max = s_max;
   // TMA loads need 16-byte aligned bases and strides; 8-byte aligned data uses cp.async
-  a.use_tma = strides16(p, k_pages, v_pages) && encode_kv_map(&a.k_map, k_pages, p, false) &&
-              encode_kv_map(&a.v_map, v_pages, p, true);
+  a.use_tma = strides16(p, k_pages, v_pages);
+  for (int m = 0; m < 4 && a.use_tma; ++m) {
+    const unsigned slots = 128u >> m;
+    a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots) &&
+                encode_kv_map(&a.v_maps[m], v_pages, p, true, slots);
+  }
   const long long stall = g_stall_next.exchange(0);
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;

@@ -10,9 +10,10 @@ namespace pa {
 // Split-KV kernel arguments (both element formats).
 struct SplitArgs {
   // 4-D byte views (row byte, KV head, slot, page) of K and V for the TMA
-  // loaders; filled when use_tma != 0 (16-byte aligned bases and strides)
-  CUtensorMap k_map;
-  CUtensorMap v_map;
+  // loaders, with boxes of 128 bytes x 128, 64, 32 and 16 slots; filled when
+  // use_tma != 0 (16-byte aligned bases and strides)
+  CUtensorMap k_maps[4];
+  CUtensorMap v_maps[4];
   int use_tma;
   const void* q;               // FP16 (E4M3 path) or BF16 (BF16 path) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs

@@ -32,6 +32,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (try_wait may suspend the thread
+// for a while before it reports an incomplete phase; a scheduler that polls
+// several barriers must not be held up by one of them).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Default bound on every pipeline wait, in SM clock cycles (about one second
 // at the GB300 clock).  A healthy wait in these kernels takes microseconds; a
 // wait that reaches the bound means a broken pipeline, and the caller

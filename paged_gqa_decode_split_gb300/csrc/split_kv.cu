@@ -79,20 +79,16 @@ struct Bf16Fmt {
   }
 };
 
-constexpr int kStages = 4;         // staging ring depth per tensor, in 32-key chunks
-constexpr int kChunkKeys = 32;
-constexpr int kPageSeg = 8;       // chunks whose page ids a loader lane holds in registers
+constexpr int kChunkKeys = 32;     // one chunk = one quarter of a tile = the keys of one decode warp
+constexpr int kPageSeg = 8;       // chunks whose page ids a cp.async loader lane holds in registers
+constexpr int kStageBytes = kTileKeys * 256;  // one tile of 256-byte key rows
 constexpr float kTau = 8.0f;       // a row's reference max moves only when a score exceeds it by 2^8
 constexpr float kNoMax = -1e30f;   // reference max of a row that has seen no key (finite: 2^(s - kNoMax) never NaN)
 constexpr int kThreads = 512;
-
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                         // up to 4 atoms x 64 rows x 128 B
-constexpr int kOffV = 32768;                     // up to 4 atoms x 128 keys x 128 B
-constexpr int kOffP = kOffV + 65536;             // 2 x (128 keys x 128 B)
-constexpr int kOffKst = kOffP + 2 * 16384;       // kStages x 32 keys x 256 B
-constexpr int kOffVst = kOffKst + kStages * 8192;
-constexpr int kOffMisc = kOffVst + kStages * 8192;
+constexpr int kSmemLimit = 232448; // opt-in shared memory per block on sm_103a (227 KB)
+constexpr int kMaxVSlots = 8;
+constexpr int kPBufs = 3;         // P^T buffers: softmax(j) writes while PV(j-1) and PV(j-2) may still read theirs
+constexpr int kSoftmaxBar = 1;     // named barrier of the four softmax warps (0 is __syncthreads)
 
 // TMEM column map (512 columns allocated)
 constexpr uint32_t kColS = 0;     // S^T, 2 buffers of 64 columns
@@ -100,21 +96,46 @@ constexpr uint32_t kColO = 128;   // O^T, d 0..127 at +0, d 128..255 at +64
 constexpr uint32_t kColK = 256;   // K' operand, 2 buffers of 128 columns
 
 struct Misc {
-  uint64_t kst_full[kStages], kst_empty[kStages], vst_full[kStages], vst_empty[kStages];
-  uint64_t kbuf_full[2], kbuf_empty[2], s_full[2], s_empty[2], p_full[2], pv_done[2];
-  uint64_t vbuf_full, q_full, q_empty, o_free, grp, fin;
+  uint64_t kst_full, kst_empty, vst_full, vst_empty;  // the K and V staging tiles
+  uint64_t kbuf_full[2], s_full[2], vtile_full[2], p_full[kPBufs], pv_done[kPBufs];
+  uint64_t q_full, q_empty, o_free, fin;
   uint32_t tmem_base;
   WaitCtl ctl;
-  int exceed_tag[2][4];
-  int rescale_tag;
+  alignas(16) int vote[2][4];        // per-warp vote words of the softmax group, double-buffered
   alignas(16) float mref[kMaxRows];  // read as float4
-  alignas(16) float thr[kMaxRows];   // (mref + tau) / c: scores above this need a new reference
-  alignas(16) float alpha[kMaxRows];
+  alignas(16) float alpha[16];
   alignas(16) float red[4][kMaxRows];
   Sched sched;
 };
 static_assert(offsetof(Misc, mref) % 16 == 0, "mref is read with 16-byte loads");
-constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;
+
+// Shared memory map (offsets from a 1024-byte aligned base) for one element
+// format and packed-row count NM:
+//   Q    K-major Q tile, D/64 atoms of NM rows x 128 B
+//   P    kPBufs P^T buffers, 128 keys x 128 B (MN-major, up to 64 rows)
+//   Kst  K staging tile, 128 keys x 256 B
+//   Vst  V staging tile, the same
+//   V    V' ring: slots of one 32-key quarter, D/64 atoms of 32 keys x 128 B,
+//        as many as fit (a quarter is released as soon as its PV MMAs finish)
+template <class Fmt, int NM>
+struct Layout {
+  static constexpr int kQAtom = NM * 128;
+  static constexpr int kQBytes = (Fmt::D / 64) * kQAtom;
+  static constexpr int kVAtom = kChunkKeys * 128;
+  static constexpr int kVQuarter = (Fmt::D / 64) * kVAtom;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffP = kQBytes;
+  static constexpr int kOffKst = kOffP + kPBufs * 16384;
+  static constexpr int kOffVst = kOffKst + kStageBytes;
+  static constexpr int kOffV = kOffVst + kStageBytes;
+  static constexpr int kVFit = (kSmemLimit - kOffV - (int)sizeof(Misc) - 1024) / kVQuarter;
+  static constexpr int kVSlots = kVFit < kMaxVSlots ? kVFit : kMaxVSlots;
+  static constexpr int kOffMisc = kOffV + kVSlots * kVQuarter;
+  static constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;
+  static_assert(kQAtom % 1024 == 0, "Q atoms must keep the 1024-byte swizzle alignment");
+  static_assert(kVSlots >= 4, "the V' ring must hold a whole tile");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory map exceeds the per-block limit");
+};
 
 // Cross-lane reduction of n per-lane values (one per packed row) in a warp.
 // Each step pairs lanes l and l^mask: while the value count is even the pair
@@ -205,48 +226,122 @@ __device__ __forceinline__ int tiles_of(const Item& x) { return (x.t1 - x.t0 + k
 __device__ __forceinline__ void load_stage_row(const uint8_t* stage, int kk, bool live, uint4 (&raw)[16]) {
 #pragma unroll
   for (int p = 0; p < 16; ++p)
-    raw[p] = live ? *reinterpret_cast<const uint4*>(stage + (p >> 3) * 4096 + kk * 128 + (((p & 7) ^ (kk & 7)) << 4))
+    raw[p] = live ? *reinterpret_cast<const uint4*>(stage + (p >> 3) * 16384 + kk * 128 + (((p & 7) ^ (kk & 7)) << 4))
                   : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// K or V loader: 32-key chunks into the staging ring.  Chunk c of the CTA's
-// item sequence goes to stage c % kStages.  Stage layout: two halves of the
-// 256-byte key rows, half h at h*4096, key kk's 128 bytes at kk*128 with its
-// 16-byte piece p at ((p ^ (kk & 7)) * 16) (the TMA 128-byte swizzle), so the
-// decode warps read eight consecutive keys without bank conflicts.
-//
-// TMA mode (16-byte aligned bases and strides): one thread issues, per 16-key
-// block, two 2 KB boxes (row bytes 0-127 and 128-255) of the 4-D byte view
-// (row byte, KV head, slot, page); completion is counted in bytes on the
-// stage's full barrier.  Blocks entirely past the split end are not loaded.
-// cp.async mode (8-byte aligned data): every lane copies 8-byte pieces of the
-// chunk's rows into the same layout, zero-filling rows past the split end.
-template <int USE_TMA>
-__device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is_v, int lane) {
+// K and V loaders: one tile (128 keys) at a time into the tensor's staging
+// tile.  Layout: two halves of the 256-byte key rows, half h at h*16384, key
+// kk's 128 bytes at kk*128 with its 16-byte piece p at ((p ^ (kk & 7)) * 16)
+// (the TMA 128-byte swizzle), so the decode warps read eight consecutive keys
+// without bank conflicts.  The tile is refilled once all four decode warps
+// have copied their rows out.  Keys past the split end may hold anything; the
+// decode warps zero them.
+
+// Block-table entry, loaded where it stands in the program (not sunk to its
+// first use), so that the loader can fetch page ids ahead of need.
+__device__ __forceinline__ int ld_page_id(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// TMA mode (16-byte aligned bases and strides): one thread.  The tile's keys
+// are cut at page boundaries; each piece (a multiple of 16 slots inside one
+// page) is covered by boxes of 128, 64, 32 and 16 slots of the 4-D byte view
+// (row byte, KV head, slot, page), two boxes (row bytes 0-127 and 128-255)
+// per piece of slots, so a tile inside one page is two copies.  Completion is
+// counted in bytes on the tile's full barrier; the thread arrives with the
+// byte total after issuing the copies.  Page ids are kept for the current
+// page index and the three after it, each loaded several pages ahead.  The
+// thread issues few instructions per tile: the shared per-SM instruction
+// queues are busy with the decode warps' traffic.
+__device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, bool is_v, uint8_t* stage) {
+  const CUtensorMap* maps = is_v ? a.v_maps : a.k_maps;  // boxes of 128, 64, 32, 16 slots
+  uint64_t* full = is_v ? &M.vst_full : &M.kst_full;
+  uint64_t* empty = is_v ? &M.vst_empty : &M.kst_empty;
+  WaitCtl* abort = &M.ctl;
+  const int ps = a.page_size;
+  const uint32_t dst_base = smem_u32(stage);
+  uint32_t j = 0;
+  for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
+    const Item x = sched_item(M.sched, a.B, it);
+    const int32_t* bt = a.block_table + (size_t)x.b * a.mpr;
+    const int nt = tiles_of(x);
+    const int q_last = (x.t1 - 1) / ps;  // last page index the item reads
+    int q_cur = x.t0 / ps;
+    int pq[4];                           // page ids of page indices q_cur .. q_cur+3 (-1 past q_last)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pq[k] = q_cur + k <= q_last ? ld_page_id(bt + q_cur + k) : -1;
+    for (int jl = 0; jl < nt; ++jl, ++j) {
+      const int kb = x.t0 + jl * kTileKeys;
+      const int rows = (min(kb + kTileKeys, x.t1) - kb + 15) & ~15;  // whole 16-key blocks holding split keys
+      if (!mbar_wait(empty, (j & 1) ^ 1, abort)) return;
+      uint32_t bytes = 0;
+      bool bad = false;
+      for (int r = 0; r < rows;) {
+        const int t = kb + r;
+        const int q = t / ps;
+        const int slot = t - q * ps;
+        const int len = min(rows - r, ps - slot);  // a multiple of 16
+        for (int adv = 0; adv < kTileKeys / 16 && q_cur < q; ++adv) {
+          pq[0] = pq[1], pq[1] = pq[2], pq[2] = pq[3];
+          ++q_cur;
+          pq[3] = q_cur + 3 <= q_last ? ld_page_id(bt + q_cur + 3) : -1;
+        }
+        const int pg = pq[0];
+        if ((unsigned)pg < (unsigned)a.num_pages) {
+          int rr = r, sl = slot, left = len;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int box = kTileKeys >> m;  // 128, 64, 32, 16 slots
+            while (left >= box) {
+              tma_load_4d(dst_base + rr * 128, maps + m, 0, x.g, sl, pg, full);
+              tma_load_4d(dst_base + 16384 + rr * 128, maps + m, 128, x.g, sl, pg, full);
+              bytes += box * 256;
+              rr += box, sl += box, left -= box;
+            }
+          }
+        } else {
+          bad = true;
+        }
+        r += len;
+      }
+      if (bad) {
+        atomicOr(a.status, 0x1u);
+        atomicOr(a.bad + x.b, 1u);
+      }
+      mbar_arrive_expect_tx(full, bytes);
+    }
+  }
+}
+
+// cp.async mode (8-byte aligned data): every lane copies 8-byte pieces of
+// the tile's rows into the same layout, zero-filling rows past the split end,
+// 32 keys at a time.  Lane l holds the page ids of key t0 + 32*cj + l for
+// eight 32-key chunks at a time: `cur` serves chunks cs..cs+7 while `nxt` is
+// being loaded for cs+8..cs+15.
+__device__ __forceinline__ void role_loader_cp(const SplitArgs& a, Misc& M, bool is_v, int lane, uint8_t* stage) {
   const uint8_t* base = is_v ? a.v : a.k;
   const long long pstr = is_v ? a.v_ps : a.k_ps;
   const long long tstr = is_v ? a.v_ts : a.k_ts;
   const long long hstr = is_v ? a.v_hs : a.k_hs;
-  const CUtensorMap* map = is_v ? &a.v_map : &a.k_map;
-  uint64_t* full = is_v ? M.vst_full : M.kst_full;
-  uint64_t* empty = is_v ? M.vst_empty : M.kst_empty;
-  uint8_t* ring = smem_base() + (is_v ? kOffVst : kOffKst);
+  uint64_t* full = is_v ? &M.vst_full : &M.kst_full;
+  uint64_t* empty = is_v ? &M.vst_empty : &M.kst_empty;
   WaitCtl* abort = &M.ctl;
-  uint32_t c = 0;
+  const uint32_t dst_base = smem_u32(stage);
+  uint32_t j = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
     const int32_t* bt = a.block_table + (size_t)x.b * a.mpr;
     const uint8_t* hbase = base + (long long)x.g * hstr;
     const int nchunks = tiles_of(x) * (kTileKeys / kChunkKeys);
-    // Page id of key t0 + 32*cj + lane, for 8 chunks at a time in registers:
-    // `cur` serves chunks cs..cs+7 while `nxt` is being loaded for cs+8..cs+15,
-    // so the block-table latency (long under full HBM load) stays hidden.
     auto load_segment = [&](int (&pg)[kPageSeg], int cs) {
 #pragma unroll
       for (int s = 0; s < kPageSeg; ++s) {
         const int cj = cs + s;
         const int t = x.t0 + cj * kChunkKeys + lane;
-        pg[s] = (cj < nchunks && t < x.t1) ? __ldg(bt + t / a.page_size) : -1;
+        pg[s] = (cj < nchunks && t < x.t1) ? ld_page_id(bt + t / a.page_size) : -1;
       }
     };
     int cur[kPageSeg], nxt[kPageSeg];
@@ -257,59 +352,34 @@ __device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is
       for (int s = 0; s < kPageSeg; ++s) {
         const int ci = cs + s;
         if (ci >= nchunks) break;
-        const int st = c % kStages;
-        const uint32_t ph = (c / kStages) & 1;
+        const int q4 = ci & 3;  // quarter of the tile
+        if (q4 == 0 && !mbar_wait(empty, (j & 1) ^ 1, abort)) goto done;
         const int page_cur = cur[s];
-        if (!mbar_wait(&empty[st], ph ^ 1, abort)) goto done;
         const int kb = x.t0 + ci * kChunkKeys;
-        const uint32_t dst0 = smem_u32(ring + st * (kChunkKeys * 256));
-        if constexpr (USE_TMA) {
-          // lanes 0 and 16 hold the pages of the chunk's two 16-key blocks
-          const int t = kb + lane;
-          bool ok = (lane & 15) == 0 && t < x.t1;
-          if (ok && (unsigned)page_cur >= (unsigned)a.num_pages) {
+        const int t = kb + lane;
+        long long rowoff = -1;
+        if (t < x.t1) {
+          if ((unsigned)page_cur < (unsigned)a.num_pages) {
+            rowoff = (long long)page_cur * pstr + (long long)(t % a.page_size) * tstr;
+          } else {
             atomicOr(a.status, 0x1u);
             atomicOr(a.bad + x.b, 1u);
-            ok = false;
           }
-          const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-          const int pg0 = __shfl_sync(0xffffffffu, page_cur, 0), pg1 = __shfl_sync(0xffffffffu, page_cur, 16);
-          if (lane == 0) {
-            const uint32_t blocks = (okmask & 1u) + ((okmask >> 16) & 1u);
-            mbar_arrive_expect_tx(&full[st], 4096u * blocks);
-#pragma unroll
-            for (int sb = 0; sb < 2; ++sb) {
-              if (!(okmask >> (16 * sb) & 1u)) continue;
-              const int pg = sb ? pg1 : pg0;
-              const int slot = (kb + 16 * sb) % a.page_size;
-              tma_load_4d(dst0 + sb * 2048, map, 0, x.g, slot, pg, &full[st]);
-              tma_load_4d(dst0 + 4096 + sb * 2048, map, 128, x.g, slot, pg, &full[st]);
-            }
-          }
-          __syncwarp();
-        } else {
-          const int t = kb + lane;
-          long long rowoff = -1;
-          if (t < x.t1) {
-            if ((unsigned)page_cur < (unsigned)a.num_pages) {
-              rowoff = (long long)page_cur * pstr + (long long)(t % a.page_size) * tstr;
-            } else {
-              atomicOr(a.status, 0x1u);
-              atomicOr(a.bad + x.b, 1u);
-            }
-          }
-#pragma unroll 4
-          for (int kk = 0; kk < kChunkKeys; ++kk) {
-            const long long ro = __shfl_sync(0xffffffffu, rowoff, kk);
-            const int piece = lane >> 1;  // 16-byte piece 0..15 of the row
-            const uint8_t* src = ro >= 0 ? hbase + ro + lane * 8 : base;
-            const uint32_t dst =
-                dst0 + (piece >> 3) * 4096 + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4) + (lane & 1) * 8;
-            cp_async_8(dst, src, ro >= 0 ? 8u : 0u);
-          }
-          cp_async_arrive(&full[st]);
         }
-        ++c;
+#pragma unroll 4
+        for (int kq = 0; kq < kChunkKeys; ++kq) {
+          const long long ro = __shfl_sync(0xffffffffu, rowoff, kq);
+          const int kk = 32 * q4 + kq;  // key of the tile
+          const int piece = lane >> 1;  // 16-byte piece 0..15 of the row
+          const uint8_t* src = ro >= 0 ? hbase + ro + lane * 8 : base;
+          const uint32_t dst =
+              dst_base + (piece >> 3) * 16384 + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4) + (lane & 1) * 8;
+          cp_async_8(dst, src, ro >= 0 ? 8u : 0u);
+        }
+        if (q4 == 3) {
+          cp_async_arrive(full);
+          ++j;
+        }
       }
 #pragma unroll
       for (int s = 0; s < kPageSeg; ++s) cur[s] = nxt[s];
@@ -317,16 +387,15 @@ __device__ __forceinline__ void role_loader(const SplitArgs& a, Misc& M, bool is
     }
   }
 done:
-  if constexpr (!USE_TMA) cp_async_wait_all();
+  cp_async_wait_all();
 }
 
 // Q loader: packed row r = qi * G + hl holds query head g*G + hl of verify
-// query qi.  K-major operand: element (r, d) at (d/64)*8192 + r*128 +
+// query qi.  K-major operand: element (r, d) at (d/64)*(NM*128) + r*128 +
 // ((((d%64)/8) ^ (r%8)) * 16) + (d%8)*2.
-template <class Fmt>
-__device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane) {
+template <class Fmt, int NM>
+__device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane, uint8_t* qbuf) {
   constexpr int kPieces = Fmt::D / 8;  // 16-byte pieces per Q row
-  uint8_t* qbuf = smem_base() + kOffQ;
   WaitCtl* abort = &M.ctl;
   const uint16_t* q = reinterpret_cast<const uint16_t*>(a.q);
   uint32_t n = 0;
@@ -337,7 +406,7 @@ __device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane
       const int r = u / kPieces, c = u % kPieces;  // piece c holds d = 8c .. 8c+7
       const int qi = r / a.G, hl = r % a.G;
       const uint16_t* src = q + ((size_t)(x.b * a.q_len + qi) * a.Hq + x.g * a.G + hl) * Fmt::D + c * 8;
-      const uint32_t dst = smem_u32(qbuf + (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+      const uint32_t dst = smem_u32(qbuf + (c >> 3) * (NM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
       cp_async_16(dst, src, 16u);
     }
     // the tensor core reads Q through the async proxy: land the copies, fence,
@@ -353,23 +422,23 @@ __device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane
 // K decode: warp quarter i owns TMEM lanes 32i..32i+31 = keys 32i.. of each
 // tile; lane = key, column c holds elements d = 2c, 2c+1.
 template <class Fmt>
-__device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb) {
-  uint8_t* ring = smem_base() + kOffKst;
+__device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb,
+                                             const uint8_t* ring) {
   WaitCtl* abort = &M.ctl;
   uint32_t j = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
     for (int jl = 0; jl < nt; ++jl, ++j) {
-      const uint32_t c = 4 * j + i;
-      const int st = c % kStages;
-      if (!mbar_wait(&M.kst_full[st], (c / kStages) & 1, abort)) return;
+      if (!mbar_wait(&M.kst_full, j & 1, abort)) return;
       // take this key's 256-byte row into registers and hand the stage back
       // at once, so the loader's refill does not wait for the tensor core
       uint4 raw[16];
-      load_stage_row(ring + st * (kChunkKeys * 256), lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
-      mbar_arrive(&M.kst_empty[st]);
-      if (!mbar_wait(&M.kbuf_empty[j & 1], ((j >> 1) & 1) ^ 1, abort)) return;
+      load_stage_row(ring, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.kst_empty);
+      // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
+      if (j >= 2 && !mbar_wait(&M.s_full[j & 1], ((j >> 1) & 1) ^ 1, abort)) return;
       const uint32_t taddr = tb + ((uint32_t)(32 * i) << 16) + kColK + (j & 1) * 128;
       if constexpr (Fmt::kElemBytes == 1) {
 #pragma unroll
@@ -399,13 +468,16 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
   }
 }
 
-// V decode: keys 32i.. of each tile into the MN-major V' operand: element
-// (key, d) at (d/64)*16384 + key*128 + ((((d%64)/8) ^ (key%8)) * 16) + (d%8)*2.
-template <class Fmt>
-__device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i, int lane) {
-  uint8_t* sm = smem_base();
-  uint8_t* ring = sm + kOffVst;
-  uint8_t* vbuf = sm + kOffV;
+// V decode: warp quarter i converts keys 32i.. of each tile, i.e. quarter
+// c = 4j + i of the CTA's key sequence, into slot c % kVSlots of the V' ring.
+// MN-major V' operand: element (key kq of the quarter, d) at (d/64)*4096 +
+// kq*128 + ((((d%64)/8) ^ (kq%8)) * 16) + (d%8)*2.  A slot is rewritten once
+// the PV of the tile that read its previous quarter has completed; the four
+// warps signal the tile's quarters on one barrier.
+template <class Fmt, int NM>
+__device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i, int lane, const uint8_t* ring,
+                                             uint8_t* vring) {
+  using L = Layout<Fmt, NM>;
   WaitCtl* abort = &M.ctl;
   uint32_t j = 0;
   const int key = 32 * i + lane;
@@ -414,13 +486,19 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
     const int nt = tiles_of(x);
     for (int jl = 0; jl < nt; ++jl, ++j) {
       const uint32_t c = 4 * j + i;
-      const int st = c % kStages;
-      if (!mbar_wait(&M.vst_full[st], (c / kStages) & 1, abort)) return;
-      // row into registers, stage back to the loader, then wait for PV(j-1)
+      if (!mbar_wait(&M.vst_full, j & 1, abort)) return;
+      // row into registers, stage back to the loader, then wait for the slot
       uint4 raw[16];
-      load_stage_row(ring + st * (kChunkKeys * 256), lane, x.t0 + jl * kTileKeys + key < x.t1, raw);
-      mbar_arrive(&M.vst_empty[st]);
-      if (j > 0 && !mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
+      load_stage_row(ring, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.vst_empty);
+      const int slot = (int)(c % L::kVSlots);
+      if (c >= (uint32_t)L::kVSlots) {
+        // the slot's previous quarter belongs to tile t; PV(t) done frees it
+        const uint32_t t = (c - L::kVSlots) / 4;
+        if (!mbar_wait(&M.pv_done[t % kPBufs], (t / kPBufs) & 1, abort)) return;
+      }
+      uint8_t* dst0 = vring + slot * L::kVQuarter + lane * 128;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         const uint4 x4 = raw[ch];
@@ -429,81 +507,94 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
           uint32_t w[8];
           Fmt::decode16(x4, w);
           const int at = ch >> 2, u = ch & 3;
-          uint8_t* dst = vbuf + at * 16384 + key * 128;
-          *reinterpret_cast<uint4*>(dst + (((2 * u) ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(dst + (((2 * u + 1) ^ (key & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          uint8_t* dst = dst0 + at * L::kVAtom;
+          *reinterpret_cast<uint4*>(dst + (((2 * u) ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(dst + (((2 * u + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
         } else {
           // piece ch = d 8ch .. 8ch+7
           const uint4 h = make_uint4(Fmt::bf2_to_h2(x4.x), Fmt::bf2_to_h2(x4.y), Fmt::bf2_to_h2(x4.z),
                                      Fmt::bf2_to_h2(x4.w));
           const int at = ch >> 3, u = ch & 7;
-          *reinterpret_cast<uint4*>(vbuf + at * 16384 + key * 128 + ((u ^ (key & 7)) << 4)) = h;
+          *reinterpret_cast<uint4*>(dst0 + at * L::kVAtom + ((u ^ (lane & 7)) << 4)) = h;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&M.vbuf_full);
+      if (lane == 0) mbar_arrive(&M.vtile_full[j & 1]);
     }
   }
 }
 
-// MMA issuer (one thread).  QK of tile j is issued before PV of tile j-1 so
-// the tensor core computes the next scores while the softmax warps work.
+// MMA issuer (one thread).  It follows the data flow with blocking waits: QK
+// of the first two tiles, then for every tile j, once the softmax has written
+// P^T(j) (which also frees S[j&1]): QK(j+2), then PV(j) once the tile's V'
+// quarters are written (on an item's first tile also after the epilogue
+// released O).  Completion is reported with few commits: QK(j) to s_full
+// (which also frees K'[j&1]), an item's last QK to q_empty, PV(j) to pv_done
+// (which also frees P^T(j) and the V' slots of tile j).  Few waits and
+// commits per tile keep the thread clear of the per-SM shared-memory queues,
+// which the decode warps keep busy.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t tb) {
-  uint8_t* sm = smem_base();
-  const uint32_t qbase = smem_u32(sm + kOffQ);
-  const uint32_t vbase = smem_u32(sm + kOffV);
-  const uint32_t pbase = smem_u32(sm + kOffP);
+__device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t tb, uint32_t qbase, uint32_t pbase,
+                                         uint32_t vbase) {
+  using L = Layout<Fmt, NM>;
   constexpr uint32_t id_qk = idesc_f16(128, NM, Fmt::kQBf16, 0, 0);
   constexpr uint32_t id_pv = idesc_f16(128, NM, 0, 1, 1);
   constexpr int kKSteps = Fmt::D / 16;
   constexpr int kHalves = Fmt::D / 128;
   WaitCtl* abort = &M.ctl;
-  uint32_t j = 0, n = 0;
-  bool ok = true;
-  auto issue_pv = [&](uint32_t jj, bool first) -> bool {
-    if (!mbar_wait(&M.p_full[jj & 1], (jj >> 1) & 1, abort)) return false;
-    if (!mbar_wait(&M.vbuf_full, jj & 1, abort)) return false;
-    if (first && !mbar_wait(&M.o_free, (n & 1) ^ 1, abort)) return false;
+  const int total = M.sched.total;
+  // QK cursor: item number qn (item index q_it), local tile q_jl of q_nt, CTA tile qj
+  int qn = 0, q_it = blockIdx.x, q_jl = 0;
+  int q_nt = q_it < total ? tiles_of(sched_item(M.sched, a.B, q_it)) : 0;
+  uint32_t qj = 0;
+  auto issue_qk = [&]() -> bool {  // QK of the cursor's tile, then advance; false on a wait that ran out
+    if (q_jl == 0 && !mbar_wait(&M.q_full, qn & 1, abort)) return false;
+    if (!mbar_wait(&M.kbuf_full[qj & 1], (qj >> 1) & 1, abort)) return false;
     tc_fence_after();
 #pragma unroll
-    for (int h = 0; h < kHalves; ++h) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sdesc_sw128(vbase + 2 * h * 16384 + kk * 2048, 16384, 1024);
-        const uint64_t bd = sdesc_sw128(pbase + (jj & 1) * 16384 + kk * 2048, 16384, 1024);
-        mma_ss(tb + kColO + 64 * h, ad, bd, id_pv, (first && kk == 0) ? 0u : 1u);
-      }
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      const uint64_t bd = sdesc_sw128(qbase + (kk >> 2) * L::kQAtom + (kk & 3) * 32, 16, 1024);
+      mma_ts(tb + kColS + (qj & 1) * 64, tb + kColK + (qj & 1) * 128 + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
     }
-    mma_commit(&M.pv_done[jj & 1]);
+    mma_commit(&M.s_full[qj & 1]);
+    if (q_jl == q_nt - 1) mma_commit(&M.q_empty);
+    ++qj;
+    if (++q_jl == q_nt) {
+      q_jl = 0;
+      ++qn;
+      q_it += gridDim.x;
+      q_nt = q_it < total ? tiles_of(sched_item(M.sched, a.B, q_it)) : 0;
+    }
     return true;
   };
-  for (int it = blockIdx.x; ok && it < M.sched.total; it += gridDim.x, ++n) {
-    const Item x = sched_item(M.sched, a.B, it);
-    const int nt = tiles_of(x);
-    if (!mbar_wait(&M.q_full, n & 1, abort)) break;
-    for (int jl = 0; jl < nt; ++jl, ++j) {
-      if (!mbar_wait(&M.kbuf_full[j & 1], (j >> 1) & 1, abort) ||
-          !mbar_wait(&M.s_empty[j & 1], ((j >> 1) & 1) ^ 1, abort)) {
-        ok = false;
-        break;
-      }
+  for (int k = 0; k < 2 && q_it < total; ++k)
+    if (!issue_qk()) return;
+  uint32_t pj = 0;
+  for (int n = 0, it = blockIdx.x; it < total; ++n, it += gridDim.x) {
+    const int nt = tiles_of(sched_item(M.sched, a.B, it));
+    for (int jl = 0; jl < nt; ++jl, ++pj) {
+      const uint32_t pb = pj % kPBufs, pu = pj / kPBufs;
+      if (!mbar_wait(&M.p_full[pb], pu & 1, abort)) return;
+      if (q_it < total && !issue_qk()) return;  // S[j&1] was read for the last time before P^T(j) was signalled
+      if (jl == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, abort)) return;
+      if (!mbar_wait(&M.vtile_full[pj & 1], (pj >> 1) & 1, abort)) return;
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kKSteps; ++kk) {
-        const uint64_t bd = sdesc_sw128(qbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        mma_ts(tb + kColS + (j & 1) * 64, tb + kColK + (j & 1) * 128 + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
+      for (int pq = 0; pq < 4; ++pq) {
+        const uint32_t vq = vbase + ((4 * pj + pq) % L::kVSlots) * L::kVQuarter;
+#pragma unroll
+        for (int h = 0; h < kHalves; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t ad = sdesc_sw128(vq + 2 * h * L::kVAtom + kk * 2048, L::kVAtom, 1024);
+            const uint64_t bd = sdesc_sw128(pbase + pb * 16384 + (2 * pq + kk) * 2048, 16384, 1024);
+            mma_ss(tb + kColO + 64 * h, ad, bd, id_pv, (jl == 0 && pq == 0 && kk == 0) ? 0u : 1u);
+          }
+        }
       }
-      mma_commit(&M.s_full[j & 1]);
-      mma_commit(&M.kbuf_empty[j & 1]);
-      if (jl == nt - 1) mma_commit(&M.q_empty);
-      if (jl > 0 && !issue_pv(j - 1, jl == 1)) {
-        ok = false;
-        break;
-      }
+      mma_commit(&M.pv_done[pb]);
     }
-    if (ok && !issue_pv(j - 1, nt == 1)) ok = false;
   }
 }
 
@@ -511,29 +602,39 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
 //
 // Scores stay in S units (the raw QK^T accumulator); c = log2(e) * scale turns
 // them into the log2 domain inside one FFMA.  Per row r the group keeps a
-// reference max m_r (log2 units; kNoMax before any visible key) and the
-// threshold thr_r = (m_r + tau) / c: a tile needs a new reference only if some
-// visible score exceeds thr_r, so the common tile is P = 2^(S*c - m_r) with no
-// cross-lane reduction.  Each thread keeps the running row sums of its own key
-// slot for all rows and the group reduces them once per item.
+// reference max m_r (log2 units; kNoMax before any visible key).  One pass per
+// 16-row chunk of a tile: x = S*c - m_r; a vote of the four warps (a named
+// barrier) checks x <= tau for every visible score, and then P = 2^x is
+// written as FP16 (at most 2^tau) with no cross-lane reduction.  A chunk whose
+// vote fails takes the row maxima of the tile, moves the references, rescales
+// the row sums and the O^T columns of those rows, and recomputes x.  Each
+// thread keeps the running row sums of its own key slot for all rows and the
+// group reduces them once per item.  Every wait is bounded; a wait that runs
+// out is reported through the next vote, so the four warps always leave
+// together and never strand one another at a barrier.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb) {
+__device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb,
+                                             uint8_t* pbuf) {
   using BF = Butterfly<NM, 16>;
+  using BF16R = Butterfly<16, 16>;
   constexpr int CNT = BF::Count;
   constexpr int kHalves = Fmt::D / 128;
-  uint8_t* pbuf = smem_base() + kOffP;
   WaitCtl* abort = &M.ctl;
   const int gt = 32 * i + lane;  // thread index inside the softmax group
   const float c_log2 = Fmt::score_scale(a.k_scale);
   const uint32_t lane_base = tb + ((uint32_t)(32 * i) << 16);
   const int rbase = BF::base(lane);  // rows rbase .. rbase+CNT-1 of every butterfly result
-  uint32_t j = 0, gph = 0;
-  auto group_sync = [&]() -> bool {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&M.grp);
-    const bool r = mbar_wait(&M.grp, gph, abort);
-    gph ^= 1;
-    return r;
+  uint32_t j = 0, nvote = 0;
+  bool bad = false;
+  // returns bit 0: some warp saw an exceeding score, bit 1: some wait ran out
+  auto vote = [&](bool ex) -> int {
+    const int f = (__any_sync(0xffffffffu, ex) ? 1 : 0) | (__any_sync(0xffffffffu, bad) ? 2 : 0);
+    int* slot = M.vote[nvote & 1];
+    ++nvote;
+    if (lane == 0) slot[i] = f;
+    named_bar_sync(kSoftmaxBar, 128);
+    const int4 w = *reinterpret_cast<const int4*>(slot);
+    return w.x | w.y | w.z | w.w;
   };
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
@@ -543,15 +644,19 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
 #pragma unroll
     for (int r = 0; r < NM; ++r) lsum[r] = 0.f;
     for (int jl = 0; jl < nt; ++jl, ++j) {
-      if (!mbar_wait(&M.s_full[j & 1], (j >> 1) & 1, abort)) return;
+      bad |= !mbar_wait(&M.s_full[j & 1], (j >> 1) & 1, abort);
+      // P^T buffer j % kPBufs is free once PV(j - kPBufs) is done
+      const uint32_t pb = j % kPBufs;
+      if (j >= kPBufs) bad |= !mbar_wait(&M.pv_done[pb], ((j / kPBufs) - 1) & 1, abort);
       tc_fence_after();
       const uint32_t s_addr = lane_base + kColS + (j & 1) * 64;
       const int tile0 = x.t0 + jl * kTileKeys;
       const int key = tile0 + gt;
       const int vis_end = min(x.t1, lim + 1);  // keys below this are visible to every row
       const bool masked_tile = tile0 + kTileKeys > vis_end || NM > a.R;
-      // 16 scores of columns 16*c16.. from TMEM, masked to -inf where invisible
-      auto load_chunk = [&](int c16, float (&v)[16]) {
+      uint8_t* prow = pbuf + pb * 16384 + gt * 128;
+      // 16 scores of rows 16*c16.. from TMEM, masked to -inf where invisible
+      auto load_scores = [&](int c16, float (&v)[16]) {
         uint32_t r[16];
         tmem_load16(s_addr + 16 * c16, r);
 #pragma unroll
@@ -565,94 +670,76 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
           }
         }
       };
-      // pass 1: does any visible score exceed its row's threshold?
-      bool ex = false;
 #pragma unroll
       for (int c16 = 0; c16 < NM / 16; ++c16) {
         float v[16];
-        load_chunk(c16, v);
+        load_scores(c16, v);
+        float mr[16];  // the chunk's reference maxima
 #pragma unroll
         for (int k = 0; k < 16; k += 4) {
-          const float4 th = *reinterpret_cast<const float4*>(&M.thr[16 * c16 + k]);
-          ex |= (v[k] > th.x) | (v[k + 1] > th.y) | (v[k + 2] > th.z) | (v[k + 3] > th.w);
+          const float4 m = *reinterpret_cast<const float4*>(&M.mref[16 * c16 + k]);
+          mr[k] = m.x, mr[k + 1] = m.y, mr[k + 2] = m.z, mr[k + 3] = m.w;
         }
-      }
-      if (__any_sync(0xffffffffu, ex) && lane == 0) M.exceed_tag[j & 1][i] = (int)j + 1;
-      if (!group_sync()) return;
-      const int* tag = M.exceed_tag[j & 1];
-      const bool slow = tag[0] == (int)j + 1 || tag[1] == (int)j + 1 || tag[2] == (int)j + 1 || tag[3] == (int)j + 1;
-      if (slow) {
-        // tile max per row: a 16-row butterfly per chunk leaves one row per lane
-        using BF16 = Butterfly<16, 16>;
+        bool ex = false;
 #pragma unroll
-        for (int c16 = 0; c16 < NM / 16; ++c16) {
-          float v[16], mx[BF16::Half];
-          load_chunk(c16, v);
-          BF16::template run_from<true>(v, mx, lane);
-          M.red[i][16 * c16 + BF16::base(lane)] = mx[0];
-        }
-        if (!group_sync()) return;
-        if (gt < NM) {
-          const float m_old = M.mref[gt];
-          const float tmax = fmaxf(fmaxf(M.red[0][gt], M.red[1][gt]), fmaxf(M.red[2][gt], M.red[3][gt]));
-          const float m_new = fmaxf(m_old, tmax * c_log2);  // tmax = -inf keeps m_old
-          const float al = (m_new == m_old) ? 1.0f : exp2f(m_old - m_new);
-          M.mref[gt] = m_new;
-          M.thr[gt] = (m_new + kTau) / c_log2;
-          M.alpha[gt] = al;
-          if (al != 1.0f) M.rescale_tag = (int)j + 1;
-        }
-        if (!group_sync()) return;
-        if (M.rescale_tag == (int)j + 1) {
-#pragma unroll
-          for (int r = 0; r < NM; r += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&M.alpha[r]);
-            lsum[r] *= al.x, lsum[r + 1] *= al.y, lsum[r + 2] *= al.z, lsum[r + 3] *= al.w;
+        for (int k = 0; k < 16; ++k) ex |= fmaf(v[k], c_log2, -mr[k]) > kTau;
+        const int f = vote(ex);
+        if (f & 2) return;
+        if (f & 1) {
+          // tile max of the chunk's rows: a 16-row butterfly leaves one row per lane
+          float mx[BF16R::Half];
+          BF16R::template run_from<true>(v, mx, lane);
+          M.red[i][16 * c16 + BF16R::base(lane)] = mx[0];
+          named_bar_sync(kSoftmaxBar, 128);
+          if (gt < 16) {
+            const int row = 16 * c16 + gt;
+            const float m_old = M.mref[row];
+            const float tmax = fmaxf(fmaxf(M.red[0][row], M.red[1][row]), fmaxf(M.red[2][row], M.red[3][row]));
+            const float m_new = fmaxf(m_old, tmax * c_log2);  // tmax = -inf keeps m_old
+            M.mref[row] = m_new;
+            M.alpha[gt] = (m_new == m_old) ? 1.0f : exp2f(m_old - m_new);
           }
-          if (jl > 0) {
-            // O^T holds tiles < j: wait for PV(j-1), then scale column r by alpha[r]
-            if (!mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
+          named_bar_sync(kSoftmaxBar, 128);
+          bool resc = false;
+#pragma unroll
+          for (int k = 0; k < 16; k += 4) {
+            const float4 al = *reinterpret_cast<const float4*>(&M.alpha[k]);
+            lsum[16 * c16 + k] *= al.x, lsum[16 * c16 + k + 1] *= al.y;
+            lsum[16 * c16 + k + 2] *= al.z, lsum[16 * c16 + k + 3] *= al.w;
+            resc |= (al.x != 1.0f) | (al.y != 1.0f) | (al.z != 1.0f) | (al.w != 1.0f);
+          }
+          if (resc && jl > 0) {
+            // O^T holds tiles < j of this item: wait for PV(j-1), then scale
+            // columns 16*c16.. (rows of this chunk) by alpha
+            bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
             tc_fence_after();
 #pragma unroll
             for (int h = 0; h < kHalves; ++h) {
+              uint32_t r[16];
+              const uint32_t ta = lane_base + kColO + 64 * h + 16 * c16;
+              tmem_load16(ta, r);
 #pragma unroll
-              for (int c16 = 0; c16 < NM / 16; ++c16) {
-                uint32_t r[16];
-                const uint32_t ta = lane_base + kColO + 64 * h + 16 * c16;
-                tmem_load16(ta, r);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * M.alpha[16 * c16 + k]);
-                PA_TMEM_ST_X16(ta, r);
-              }
+              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * M.alpha[k]);
+              PA_TMEM_ST_X16(ta, r);
             }
             tmem_wait_st();
           }
-        }
-      }
-      // pass 2: probabilities -> P^T row of this key (MN-major: one 128-byte
-      // row per key, 8-row pieces swizzled); P[j&1] is free once PV(j-2) is
-      // done.  A masked score is -inf, so its probability is exactly 0.
-      if (j >= 2 && !mbar_wait(&M.pv_done[j & 1], ((j - 2) >> 1) & 1, abort)) return;
-      uint8_t* prow = pbuf + (j & 1) * 16384 + gt * 128;
+          load_scores(c16, v);  // reloaded rather than held across the rescale
 #pragma unroll
-      for (int c16 = 0; c16 < NM / 16; ++c16) {
-        float v[16];
-        load_chunk(c16, v);
+          for (int k = 0; k < 16; k += 4) {
+            const float4 m = *reinterpret_cast<const float4*>(&M.mref[16 * c16 + k]);
+            mr[k] = m.x, mr[k + 1] = m.y, mr[k + 2] = m.z, mr[k + 3] = m.w;
+          }
+        }
+        // probabilities with the (possibly moved) references -> the P^T row
+        // of this key (MN-major: one 128-byte row per key, 8-row pieces
+        // swizzled).  A masked score is -inf, so its probability is exactly 0.
 #pragma unroll
         for (int h8 = 0; h8 < 2; ++h8) {
           const int c8 = 2 * c16 + h8;
-          const float4 m0 = *reinterpret_cast<const float4*>(&M.mref[8 * c8]);
-          const float4 m1 = *reinterpret_cast<const float4*>(&M.mref[8 * c8 + 4]);
-          const float* u = v + 8 * h8;
           float p[8];
-          p[0] = ex2_approx(fmaf(u[0], c_log2, -m0.x));
-          p[1] = ex2_approx(fmaf(u[1], c_log2, -m0.y));
-          p[2] = ex2_approx(fmaf(u[2], c_log2, -m0.z));
-          p[3] = ex2_approx(fmaf(u[3], c_log2, -m0.w));
-          p[4] = ex2_approx(fmaf(u[4], c_log2, -m1.x));
-          p[5] = ex2_approx(fmaf(u[5], c_log2, -m1.y));
-          p[6] = ex2_approx(fmaf(u[6], c_log2, -m1.z));
-          p[7] = ex2_approx(fmaf(u[7], c_log2, -m1.w));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) p[k] = ex2_approx(fmaf(v[8 * h8 + k], c_log2, -mr[8 * h8 + k]));
           __half2 h0 = __floats2half2_rn(p[0], p[1]);
           __half2 h1 = __floats2half2_rn(p[2], p[3]);
           __half2 h2 = __floats2half2_rn(p[4], p[5]);
@@ -667,25 +754,24 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
           for (int k = 0; k < 8; ++k) lsum[8 * c8 + k] += p[k];
         }
       }
-      // S[j&1] may now be overwritten by QK(j+2)
+      // P^T buffer pb complete and any O^T rescale of this tile stored; S[j&1]
+      // was read for the last time, so QK(j+2) may overwrite it
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&M.s_empty[j & 1]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&M.p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&M.p_full[pb]);
     }
     // ---- epilogue: (m, l, O) partials of this item
     BF::template run<false>(lsum, lane);
 #pragma unroll
     for (int k = 0; k < CNT; ++k) M.red[i][rbase + k] = lsum[k];
-    if (!group_sync()) return;
+    named_bar_sync(kSoftmaxBar, 128);
     const size_t pi = panel_index(a, x);
     if (gt < a.R) {
       const float l = (M.red[0][gt] + M.red[1][gt]) + (M.red[2][gt] + M.red[3][gt]);
       a.panel_ml[pi + gt] = make_float2(l > 0.f ? M.mref[gt] : -INFINITY, l);
     }
-    if (!mbar_wait(&M.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) return;
+    bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
     tc_fence_after();
 #pragma unroll
     for (int h = 0; h < kHalves; ++h) {
@@ -703,56 +789,49 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i,
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&M.o_free);
-    if (!group_sync()) return;
-    if (gt < kMaxRows) {
-      M.mref[gt] = kNoMax;
-      M.thr[gt] = -INFINITY;
-    }
-    if (!group_sync()) return;
+    named_bar_sync(kSoftmaxBar, 128);  // every warp is done with mref and red
+    if (gt < kMaxRows) M.mref[gt] = kNoMax;
+    named_bar_sync(kSoftmaxBar, 128);
   }
 }
 
 template <class Fmt, int NM, int TMA>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitArgs a) {
+  using L = Layout<Fmt, NM>;
   uint8_t* sm = smem_base();
-  Misc& M = *reinterpret_cast<Misc*>(sm + kOffMisc);
+  Misc& M = *reinterpret_cast<Misc*>(sm + L::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&M.kst_full[s], a.use_tma ? 1 : 32);
-      mbar_init(&M.vst_full[s], a.use_tma ? 1 : 32);
-      mbar_init(&M.kst_empty[s], 32);
-      mbar_init(&M.vst_empty[s], 32);
-    }
+    mbar_init(&M.kst_full, a.use_tma ? 1 : 32);
+    mbar_init(&M.vst_full, a.use_tma ? 1 : 32);
+    mbar_init(&M.kst_empty, 4);
+    mbar_init(&M.vst_empty, 4);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&M.kbuf_full[s], 4);
-      mbar_init(&M.kbuf_empty[s], 1);
       mbar_init(&M.s_full[s], 1);
-      mbar_init(&M.s_empty[s], 4);
+      mbar_init(&M.vtile_full[s], 4);
+    }
+    for (int s = 0; s < kPBufs; ++s) {
       mbar_init(&M.p_full[s], 4);
       mbar_init(&M.pv_done[s], 1);
     }
-    mbar_init(&M.vbuf_full, 4);
     mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
     mbar_init(&M.o_free, 4);
-    mbar_init(&M.grp, 4);
     mbar_init(&M.fin, 1);
     M.ctl.abort = 0;
     M.ctl.limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
-    M.rescale_tag = 0;
-    for (int w = 0; w < 8; ++w) M.exceed_tag[w / 4][w % 4] = 0;
+    for (int w = 0; w < 8; ++w) M.vote[w / 4][w % 4] = 0;
     mbar_fence_init();
   }
-  if (tid < kMaxRows) {
-    M.mref[tid] = kNoMax;
-    M.thr[tid] = -INFINITY;
-  }
+  if (tid < kMaxRows) M.mref[tid] = kNoMax;
   if (warp == 1) tmem_alloc(&M.tmem_base, 512);
   // zero the Q tile (rows >= R stay zero) and both P^T buffers (rows >= N stay zero)
-  for (int o = tid * 16; o < 32768; o += kThreads * 16) *reinterpret_cast<uint4*>(sm + kOffQ + o) = make_uint4(0, 0, 0, 0);
-  for (int o = tid * 16; o < 32768; o += kThreads * 16) *reinterpret_cast<uint4*>(sm + kOffP + o) = make_uint4(0, 0, 0, 0);
+  for (int o = tid * 16; o < L::kQBytes; o += kThreads * 16)
+    *reinterpret_cast<uint4*>(sm + L::kOffQ + o) = make_uint4(0, 0, 0, 0);
+  for (int o = tid * 16; o < kPBufs * 16384; o += kThreads * 16)
+    *reinterpret_cast<uint4*>(sm + L::kOffP + o) = make_uint4(0, 0, 0, 0);
   sched_build(M.sched, a.ctx_lens, a.B, a.Hkv, a.max_ctx, a.status, a.bad);  // contains __syncthreads
   fence_proxy_async_smem();
   tc_fence_before();
@@ -760,15 +839,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tb = M.tmem_base;
 
-  if (warp == 0) {
-    role_loader<TMA>(a, M, false, lane);
-  } else if (warp == 2) {
-    role_loader<TMA>(a, M, true, lane);
+  if (warp == 0 || warp == 2) {
+    if constexpr (TMA) {
+      if (lane == 0) role_loader_tma(a, M, warp == 2, sm + (warp == 2 ? L::kOffVst : L::kOffKst));
+    } else {
+      role_loader_cp(a, M, warp == 2, lane, sm + (warp == 2 ? L::kOffVst : L::kOffKst));
+    }
+    __syncwarp();
   } else if (warp == 3) {
-    role_qload<Fmt>(a, M, lane);
+    role_qload<Fmt, NM>(a, M, lane, sm + L::kOffQ);
   } else if (warp == 1) {
     if (lane == 0) {
-      role_mma<Fmt, NM>(a, M, tb);
+      role_mma<Fmt, NM>(a, M, tb, smem_u32(sm + L::kOffQ), smem_u32(sm + L::kOffP), smem_u32(sm + L::kOffV));
       // drain: every issued MMA must finish before TMEM is released
       mma_commit(&M.fin);
       const long long t0 = clock64();
@@ -777,11 +859,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     }
     __syncwarp();
   } else if (warp < 8) {
-    role_kdecode<Fmt>(a, M, warp - 4, lane, tb);
+    role_kdecode<Fmt>(a, M, warp - 4, lane, tb, sm + L::kOffKst);
   } else if (warp < 12) {
-    role_vdecode<Fmt>(a, M, warp - 8, lane);
+    role_vdecode<Fmt, NM>(a, M, warp - 8, lane, sm + L::kOffVst, sm + L::kOffV);
   } else {
-    role_softmax<Fmt, NM>(a, M, warp - 12, lane, tb);
+    role_softmax<Fmt, NM>(a, M, warp - 12, lane, tb, sm + L::kOffP);
   }
 
   tc_fence_before();
@@ -795,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
 
 template <class Fmt, int NM, int TMA>
 cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
+  constexpr int kSmem = Layout<Fmt, NM>::kSmemBytes;
   auto kern = split_kernel<Fmt, NM, TMA>;
   // the attribute is per device; setting it is idempotent, so a racing second
   // setter is harmless
@@ -804,11 +887,11 @@ cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(set_on_devices.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     set_on_devices.fetch_or(bit);
   }
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(a);
+  kern<<<grid, kThreads, kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -825,7 +908,7 @@ cudaError_t launch_mode(const SplitArgs& a, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-int split_smem_bytes() { return kSmemBytes; }
+int split_smem_bytes() { return Layout<Fp8Fmt, 64>::kSmemBytes; }
 
 cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, cudaStream_t stream) {
   if (bf16) return a.use_tma ? launch_mode<Bf16Fmt, 1>(a, grid, stream) : launch_mode<Bf16Fmt, 0>(a, grid, stream);
