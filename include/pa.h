@@ -96,7 +96,8 @@ typedef struct pa_caps {
   int32_t accum_bits;    /* width of the QK and PV accumulators: 32 */
   int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8: 256 */
   int32_t bf16_head_dim; /* head_dim of pa_decode_bf16_d128: 128 */
-  int32_t reserved[7];
+  int32_t max_splits;    /* most splits one request is cut into (pa_split_plan's *num_splits) */
+  int32_t reserved[6];
 } pa_caps;
 
 /* Geometry of one call (host struct, read during the call only). */

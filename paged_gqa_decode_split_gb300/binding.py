@@ -28,7 +28,7 @@ class pa_caps(ctypes.Structure):
     _fields_ = [("abi_version", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
                 ("max_group", ctypes.c_int32), ("page_multiple", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
                 ("accum_bits", ctypes.c_int32), ("fp8_head_dim", ctypes.c_int32), ("bf16_head_dim", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 7)]
+                ("max_splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
 
 
 class pa_params(ctypes.Structure):

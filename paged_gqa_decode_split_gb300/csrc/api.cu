@@ -271,6 +271,7 @@ int pa_get_capabilities(pa_caps* out) {
   out->accum_bits = 32;
   out->fp8_head_dim = 256;
   out->bf16_head_dim = 128;
+  out->max_splits = kMaxSplits;
   return PA_OK;
 }
 

@@ -17,7 +17,7 @@ namespace pa {
 
 namespace {
 
-static_assert(kMaxSplits <= 32, "one warp computes the split weights");
+static_assert(kMaxSplits <= 64, "one warp computes the split weights, two splits per lane");
 
 template <bool BF16OUT>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
@@ -35,23 +35,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   if (a.bad != nullptr && a.bad[b] != 0u) ns = 0;
   const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
   const size_t prow = (size_t)bg * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
-  // one warp: M = max_s m_s, w_s = 2^(m_s - M), lsum = sum_s w_s l_s
+  // one warp, splits s and s + 32 on lane s: M = max_s m_s, w_s = 2^(m_s - M),
+  // lsum = sum_s w_s l_s (a fixed reduction tree, so the bits depend on ns only)
   if (threadIdx.x < 32) {
     const int s = threadIdx.x;
-    float m = -INFINITY, l = 0.f;
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
     if (s < ns) {
       const float2 ml = a.panel_ml[prow + (size_t)s * a.R];
-      m = ml.x;
-      l = ml.y;
+      m0 = ml.x, l0 = ml.y;
     }
-    float M = m;
+    if (s + 32 < ns) {
+      const float2 ml = a.panel_ml[prow + (size_t)(s + 32) * a.R];
+      m1 = ml.x, l1 = ml.y;
+    }
+    float M = fmaxf(m0, m1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-    float ls = w * l;
+    const float w0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M);
+    const float w1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - M);
+    float ls = w0 * l0 + w1 * l1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    if (s < kMaxSplits) w_s[s] = w;
+    if (s < kMaxSplits) w_s[s] = w0;
+    if (s + 32 < kMaxSplits) w_s[s + 32] = w1;
     if (s == 0) {
       lsum_s = ls;
       if (a.lse != nullptr)

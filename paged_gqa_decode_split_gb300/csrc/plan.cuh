@@ -10,7 +10,8 @@ namespace pa {
 // ------------------------------------------------------------ constants --
 constexpr int kTileKeys = 128;     // keys per tensor-core tile (MMA M dimension)
 constexpr int kSplitTarget = 512;  // a split holds about this many keys before the cap
-constexpr int kMaxSplits = 32;     // at most this many splits per request
+constexpr int kMaxSplits = 38;     // at most this many splits per request: a quarter of the 152 SMs,
+                                   // so 4, 8 or 16 long requests fill whole waves of a one-CTA-per-SM grid
 constexpr int kMaxBatch = 64;
 constexpr int kMaxQLen = 8;
 constexpr int kMaxGroup = 8;

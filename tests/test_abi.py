@@ -30,6 +30,7 @@ def test_capabilities(lib):
     assert c.accum_bits == 32
     assert c.page_multiple == 16
     assert c.fp8_head_dim == 256 and c.bf16_head_dim == 128
+    assert c.max_splits == 38 and all(r == 0 for r in c.reserved)
     assert c.max_q_len >= 8 and c.max_group >= 6 and c.max_batch >= 16 and c.max_ctx >= 262144
     assert lib.pa_get_capabilities(None) == B.PA_ERR_NULL
 
@@ -40,11 +41,12 @@ def test_status_strings(lib):
 
 
 def splits_for_len(L: int) -> tuple[int, int]:
-    """Restatement of the split policy: about 512 keys per split, at most 32
-    splits, split length a whole number of 128-key tiles."""
+    """Restatement of the split policy: about 512 keys per split, at most 38
+    splits (a quarter of the 152 SMs), split length a whole number of 128-key
+    tiles."""
     if L <= 0:
         return 0, 0
-    s0 = min(max(math.ceil(L / 512), 1), 32)
+    s0 = min(max(math.ceil(L / 512), 1), 38)
     chunk = math.ceil(math.ceil(L / s0) / 128) * 128
     return math.ceil(L / chunk), chunk
 
@@ -56,23 +58,23 @@ def test_split_plan_matches_restatement(lib, L):
     assert st == 0
     assert (s, c) == splits_for_len(L)
     if L > 0:
-        assert 1 <= s <= 32 and c % 128 == 0
+        assert 1 <= s <= 38 and c % 128 == 0
         assert (s - 1) * c < L <= s * c  # every split non-empty
 
 
 def test_split_count_bounded_by_workspace_bound(lib):
-    """The count is not monotone in L (S(16384) = 32, S(16385) = 26), so the
-    workspace is sized with the monotone bound clamp(ceil(max_ctx/512), 1, 32);
+    """The count is not monotone in L (S(19456) = 38, S(19457) = 31), so the
+    workspace is sized with the monotone bound clamp(ceil(max_ctx/512), 1, 38);
     no length up to max_ctx may need more splits than that."""
-    assert B.pa_split_plan(16384)[1] == 32 and B.pa_split_plan(16385)[1] == 26
+    assert B.pa_split_plan(19456)[1] == 38 and B.pa_split_plan(19457)[1] == 31
     worst = 0
     for L in range(0, 70000, 7):
         worst = max(worst, B.pa_split_plan(L)[1])
-        assert B.pa_split_plan(L)[1] <= min(32, max(1, math.ceil(L / 512)))
-    assert worst == 32
-    # the workspace of max_ctx_len 16385 must hold 32 splits per (request, KV head)
-    p = _params(max_ctx_len=16385, max_pages_per_req=10)
-    assert B.pa_decode_fp8_workspace_bytes(p) >= 1024 + 8 * 32 * 48 * (256 * 4 + 8)
+        assert B.pa_split_plan(L)[1] <= min(38, max(1, math.ceil(L / 512)))
+    assert worst == 38
+    # the workspace of max_ctx_len 19457 must hold 38 splits per (request, KV head)
+    p = _params(max_ctx_len=19457, max_pages_per_req=12)
+    assert B.pa_decode_fp8_workspace_bytes(p) >= 1024 + 8 * 38 * 48 * (256 * 4 + 8)
 
 
 def test_split_plan_rejects_negative(lib):
@@ -80,9 +82,10 @@ def test_split_plan_rejects_negative(lib):
 
 
 def test_split_plan_known_configs(lib):
-    assert B.pa_split_plan(131072)[1:] == (32, 4096)
+    assert B.pa_split_plan(131072)[1:] == (38, 3456)
+    assert B.pa_split_plan(32768)[1:] == (37, 896)
     assert B.pa_split_plan(3297)[1:] == (7, 512)
-    assert B.pa_split_plan(262144)[1:] == (32, 8192)
+    assert B.pa_split_plan(262144)[1:] == (38, 6912)
 
 
 def _params(**kw):
@@ -96,7 +99,7 @@ def _params(**kw):
 def test_workspace_size_formula(lib):
     p = _params()
     n = B.pa_decode_fp8_workspace_bytes(p)
-    items = 8 * 1 * 32 * 48
+    items = 8 * 1 * 38 * 48
     assert n >= 1024 + items * 8 + items * 256 * 4
     assert n % 256 == 0
     assert B.pa_decode_fp8_workspace_bytes(_params(head_dim=128)) == 0

@@ -219,7 +219,7 @@ def test_worklist_bit_exact():
     w = wl.generate(spec, 3)
     p = D.params_for(w)
     cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    cap = len(lens) * 2 * 32
+    cap = len(lens) * 2 * B.pa_get_capabilities().max_splits
     items = torch.full((cap, 4), -7, dtype=torch.int32, device="cuda")
     count = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.check(B.pa_debug_worklist(p, cl, items, cap, count), "pa_debug_worklist")
