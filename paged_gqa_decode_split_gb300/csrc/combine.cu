@@ -32,9 +32,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   if (L < 0 || L > a.max_ctx) L = 0;
   int ns, chunk;
   split_plan(L, ns, chunk);
-  if (a.bad != nullptr && a.bad[b] != 0u) ns = 0;
   const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
   const size_t prow = (size_t)bg * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
+  // everything above reads inputs only; the partials and the input flags come
+  // from the split kernel, which may still be finishing (programmatic launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.bad != nullptr && a.bad[b] != 0u) ns = 0;
+  // the partial O of every split, requested before the weights are known so
+  // that the two rounds of loads overlap
+  const float* o0 = a.panel_o + prow * a.D;
+  const size_t sstride = (size_t)a.R * a.D;
+  const int d0 = threadIdx.x;  // one thread per element d of the row (blockDim.x = D <= 256)
+  float o[kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) o[s] = (s < ns && d0 < a.D) ? __ldg(o0 + s * sstride + d0) : 0.f;
   // one warp, splits s and s + 32 on lane s: M = max_s m_s, w_s = 2^(m_s - M),
   // lsum = sum_s w_s l_s (a fixed reduction tree, so the bits depend on ns only)
   if (threadIdx.x < 32) {
@@ -67,15 +78,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   __syncthreads();
   const float lsum = lsum_s;
   const float scale = (a.out_scale_ptr ? __ldg(a.out_scale_ptr) : 1.0f) * a.out_scale_mul;
-  const float* o0 = a.panel_o + prow * a.D;
-  const size_t sstride = (size_t)a.R * a.D;
-  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+  if (d0 < a.D) {
+    const int d = d0;
     float val = 0.f;
     if (lsum > 0.f) {
-      // all loads issued up front; accumulation in ascending split order
-      float o[kMaxSplits];
-#pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s) o[s] = (s < ns) ? __ldg(o0 + s * sstride + d) : 0.f;
+      // accumulation in ascending split order
       float acc = 0.f;
 #pragma unroll
       for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(w_s[s], o[s], acc) : acc;
@@ -124,14 +131,22 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint8_t* base, long l
 
 }  // namespace
 
+// Launched as a programmatic dependent of the split kernel: its blocks may
+// be scheduled as the split kernel's blocks retire, and each waits
+// (griddepcontrol.wait) for the split kernel's completion and memory before
+// it reads a partial.
 cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream) {
-  const int grid = a.B * a.Hkv * a.R;
-  const int threads = a.D < 256 ? a.D : 256;
-  if (bf16_out)
-    combine_kernel<true><<<grid, threads, 0, stream>>>(a);
-  else
-    combine_kernel<false><<<grid, threads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * a.Hkv * a.R);
+  cfg.blockDim = dim3(a.D);  // one thread per output element of the row (D <= 256)
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return bf16_out ? cudaLaunchKernelEx(&cfg, combine_kernel<true>, a) : cudaLaunchKernelEx(&cfg, combine_kernel<false>, a);
 }
 
 cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,

@@ -168,6 +168,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of an operand `bytes` further on: the start field holds the
+// shared address >> 4 in 14 bits, and every shared address of a block is
+// below 256 KB, so the offset never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 #define PA_TMEM_LD_X16(taddr, r)                                                                                  \
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}," \
                " [%16];"                                                                                          \

@@ -548,15 +548,18 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
   int qn = 0, q_it = blockIdx.x, q_jl = 0;
   int q_nt = q_it < total ? tiles_of(sched_item(M.sched, a.B, q_it)) : 0;
   uint32_t qj = 0;
+  // operand descriptors at offset 0; each MMA adds a compile-time offset
+  const uint64_t q_desc = sdesc_sw128(qbase, 16, 1024);
+  const uint64_t v_desc = sdesc_sw128(vbase, L::kVAtom, 1024);
+  const uint64_t p_desc = sdesc_sw128(pbase, 16384, 1024);
   auto issue_qk = [&]() -> bool {  // QK of the cursor's tile, then advance; false on a wait that ran out
     if (q_jl == 0 && !mbar_wait(&M.q_full, qn & 1, abort)) return false;
     if (!mbar_wait(&M.kbuf_full[qj & 1], (qj >> 1) & 1, abort)) return false;
     tc_fence_after();
+    const uint32_t s_col = tb + kColS + (qj & 1) * 64, k_col = tb + kColK + (qj & 1) * 128;
 #pragma unroll
-    for (int kk = 0; kk < kKSteps; ++kk) {
-      const uint64_t bd = sdesc_sw128(qbase + (kk >> 2) * L::kQAtom + (kk & 3) * 32, 16, 1024);
-      mma_ts(tb + kColS + (qj & 1) * 64, tb + kColK + (qj & 1) * 128 + kk * 8, bd, id_qk, kk > 0 ? 1u : 0u);
-    }
+    for (int kk = 0; kk < kKSteps; ++kk)
+      mma_ts(s_col, k_col + kk * 8, sdesc_add(q_desc, (kk >> 2) * L::kQAtom + (kk & 3) * 32), id_qk, kk > 0 ? 1u : 0u);
     mma_commit(&M.s_full[qj & 1]);
     if (q_jl == q_nt - 1) mma_commit(&M.q_empty);
     ++qj;
@@ -571,6 +574,7 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
   for (int k = 0; k < 2 && q_it < total; ++k)
     if (!issue_qk()) return;
   uint32_t pj = 0;
+  int slot0 = 0;  // V' slot of the tile's first quarter: (4 * pj) % kVSlots
   for (int n = 0, it = blockIdx.x; it < total; ++n, it += gridDim.x) {
     const int nt = tiles_of(sched_item(M.sched, a.B, it));
     for (int jl = 0; jl < nt; ++jl, ++pj) {
@@ -580,19 +584,22 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
       if (jl == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, abort)) return;
       if (!mbar_wait(&M.vtile_full[pj & 1], (pj >> 1) & 1, abort)) return;
       tc_fence_after();
+      const uint64_t pd = sdesc_add(p_desc, pb * 16384);
+      const uint32_t first = jl == 0 ? 0u : 1u;
+      int slot = slot0;
 #pragma unroll
       for (int pq = 0; pq < 4; ++pq) {
-        const uint32_t vq = vbase + ((4 * pj + pq) % L::kVSlots) * L::kVQuarter;
+        const uint64_t vd = sdesc_add(v_desc, slot * L::kVQuarter);
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) {
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t ad = sdesc_sw128(vq + 2 * h * L::kVAtom + kk * 2048, L::kVAtom, 1024);
-            const uint64_t bd = sdesc_sw128(pbase + pb * 16384 + (2 * pq + kk) * 2048, 16384, 1024);
-            mma_ss(tb + kColO + 64 * h, ad, bd, id_pv, (jl == 0 && pq == 0 && kk == 0) ? 0u : 1u);
-          }
+          for (int kk = 0; kk < 2; ++kk)
+            mma_ss(tb + kColO + 64 * h, sdesc_add(vd, 2 * h * L::kVAtom + kk * 2048),
+                   sdesc_add(pd, (2 * pq + kk) * 2048), id_pv, (pq == 0 && kk == 0) ? first : 1u);
         }
+        slot = slot + 1 == L::kVSlots ? 0 : slot + 1;
       }
+      slot0 = slot;
       mma_commit(&M.pv_done[pb]);
     }
   }
@@ -838,6 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = M.tmem_base;
+  // the combine kernel may be launched now; it waits for this grid to finish
+  // before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == 0 || warp == 2) {
     if constexpr (TMA) {
