@@ -221,7 +221,7 @@ __device__ __forceinline__ int tiles_of(const Item& x) { return (x.t1 - x.t0 + k
 
 // ------------------------------------------------------------------ roles --
 
-// Key row kk of a stage (see role_loader) as 16 pieces of 16 bytes; zeros
+// Key row kk of a stage (see role_loader_tma) as 16 pieces of 16 bytes; zeros
 // for keys past the split end (their stage bytes are stale or a page tail).
 __device__ __forceinline__ void load_stage_row(const uint8_t* stage, int kk, bool live, uint4 (&raw)[16]) {
 #pragma unroll
