@@ -20,14 +20,15 @@
 // that P can stay FP16 in the PV product.  Each TMEM lane is one key, so the
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
-// Warp roles (16 warps):
-//   0  K loader   TMA (or cp.async for 8-byte aligned data) of block-table-
-//                 gathered K rows into a 32-key staging ring
-//   2  V loader   the same for V
-//   3  Q loader   the packed Q tile of each item (128-byte swizzle)
+// Warp roles (16 warps; warp w runs on sub-partition w % 4):
+//   3  K loader   one thread: TMA (or the warp: cp.async for 8-byte aligned
+//                 data) of block-table-gathered K rows, a tile at a time
+//   9  V loader   the same for V
+//   11 Q loader   the packed Q tile of each item (128-byte swizzle)
 //   1  MMA        one thread issues tcgen05.mma and commits to mbarriers
 //   4-7  K decode staging -> K' in TMEM (lane = key), the QK A operand
-//   8-11 V decode staging -> V' in the MN-major SMEM operand
+//   0, 8, 2, 10  V decode, key quarters 0-3: staging -> V' in a ring of
+//                MN-major SMEM quarter slots
 //   12-15 softmax masking, lazy-max online softmax, P^T, row sums, O^T rescale,
 //         and the item's FP32 (m, l, O) partials written to the workspace.
 // Every wait is bounded (see mbar_wait); a wait that runs out aborts the CTA
@@ -849,14 +850,20 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   // before it reads anything this grid writes
   asm volatile("griddepcontrol.launch_dependents;");
 
-  if (warp == 0 || warp == 2) {
+  // warp w runs on sub-partition w % 4; the TMEM lane quarter of the K decode
+  // and softmax warps is w % 4 as well.  The V decode warps, the heaviest
+  // users of the shared-memory queues, sit on sub-partitions 0 and 2, away
+  // from the MMA issuer on sub-partition 1.
+  const int vq = warp == 0 ? 0 : warp == 8 ? 1 : warp == 2 ? 2 : warp == 10 ? 3 : -1;
+  if (warp == 3 || warp == 9) {
+    const bool is_v = warp == 9;
     if constexpr (TMA) {
-      if (lane == 0) role_loader_tma(a, M, warp == 2, sm + (warp == 2 ? L::kOffVst : L::kOffKst));
+      if (lane == 0) role_loader_tma(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst));
     } else {
-      role_loader_cp(a, M, warp == 2, lane, sm + (warp == 2 ? L::kOffVst : L::kOffKst));
+      role_loader_cp(a, M, is_v, lane, sm + (is_v ? L::kOffVst : L::kOffKst));
     }
     __syncwarp();
-  } else if (warp == 3) {
+  } else if (warp == 11) {
     role_qload<Fmt, NM>(a, M, lane, sm + L::kOffQ);
   } else if (warp == 1) {
     if (lane == 0) {
@@ -868,10 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp >= 4 && warp < 8) {
     role_kdecode<Fmt>(a, M, warp - 4, lane, tb, sm + L::kOffKst);
-  } else if (warp < 12) {
-    role_vdecode<Fmt, NM>(a, M, warp - 8, lane, sm + L::kOffVst, sm + L::kOffV);
+  } else if (vq >= 0) {
+    role_vdecode<Fmt, NM>(a, M, vq, lane, sm + L::kOffVst, sm + L::kOffV);
   } else {
     role_softmax<Fmt, NM>(a, M, warp - 12, lane, tb, sm + L::kOffP);
   }
