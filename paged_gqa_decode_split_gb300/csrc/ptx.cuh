@@ -189,6 +189,17 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { r
                "r"((r)[14]), "r"((r)[15])                                                                          \
                : "memory")
 
+#define PA_TMEM_LD_X8(taddr, r)                                                                                  \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"                           \
+               : "=r"((r)[0]), "=r"((r)[1]), "=r"((r)[2]), "=r"((r)[3]), "=r"((r)[4]), "=r"((r)[5]),            \
+                 "=r"((r)[6]), "=r"((r)[7])                                                                      \
+               : "r"(taddr))
+
+#define PA_TMEM_ST_X8(taddr, r)                                                                                  \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"((r)[0]),   \
+               "r"((r)[1]), "r"((r)[2]), "r"((r)[3]), "r"((r)[4]), "r"((r)[5]), "r"((r)[6]), "r"((r)[7])            \
+               : "memory")
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

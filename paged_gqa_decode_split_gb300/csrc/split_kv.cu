@@ -20,7 +20,7 @@
 // that P can stay FP16 in the PV product.  Each TMEM lane is one key, so the
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
-// Warp roles (16 warps; warp w runs on sub-partition w % 4):
+// Warp roles (20 warps; warp w runs on sub-partition w % 4):
 //   3  K loader   one thread: TMA (or the warp: cp.async for 8-byte aligned
 //                 data) of block-table-gathered K rows, a tile at a time
 //   9  V loader   the same for V
@@ -29,7 +29,8 @@
 //   4-7  K decode staging -> K' in TMEM (lane = key), the QK A operand
 //   0, 8, 2, 10  V decode, key quarters 0-3: staging -> V' in a ring of
 //                MN-major SMEM quarter slots
-//   12-15 softmax masking, lazy-max online softmax, P^T, row sums, O^T rescale,
+//   12-15, 16-19  softmax, two groups of four, each for half of the packed
+//         rows: masking, lazy-max online softmax, P^T, row sums, O^T rescale,
 //         and the item's FP32 (m, l, O) partials written to the workspace.
 // Every wait is bounded (see mbar_wait); a wait that runs out aborts the CTA
 // cleanly, frees TMEM and raises PA_FLAG_TIMEOUT.
@@ -85,11 +86,11 @@ constexpr int kPageSeg = 8;       // chunks whose page ids a cp.async loader lan
 constexpr int kStageBytes = kTileKeys * 256;  // one tile of 256-byte key rows
 constexpr float kTau = 8.0f;       // a row's reference max moves only when a score exceeds it by 2^8
 constexpr float kNoMax = -1e30f;   // reference max of a row that has seen no key (finite: 2^(s - kNoMax) never NaN)
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kSmemLimit = 232448; // opt-in shared memory per block on sm_103a (227 KB)
 constexpr int kMaxVSlots = 8;
 constexpr int kPBufs = 3;         // P^T buffers: softmax(j) writes while PV(j-1) and PV(j-2) may still read theirs
-constexpr int kSoftmaxBar = 1;     // named barrier of the four softmax warps (0 is __syncthreads)
+constexpr int kSoftmaxBar = 1;     // named barriers 1 and 2: the two softmax groups (0 is __syncthreads)
 
 // TMEM column map (512 columns allocated)
 constexpr uint32_t kColS = 0;     // S^T, 2 buffers of 64 columns
@@ -102,9 +103,9 @@ struct Misc {
   uint64_t q_full, q_empty, o_free, fin;
   uint32_t tmem_base;
   WaitCtl ctl;
-  alignas(16) int vote[2][4];        // per-warp vote words of the softmax group, double-buffered
+  alignas(16) int vote[2][2][4];     // per-warp vote words of each softmax group, double-buffered
   alignas(16) float mref[kMaxRows];  // read as float4
-  alignas(16) float alpha[16];
+  alignas(16) float alpha[kMaxRows];
   alignas(16) float red[4][kMaxRows];
   Sched sched;
 };
@@ -606,200 +607,216 @@ __device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t t
   }
 }
 
-// Softmax warps: quarter i reads TMEM lanes 32i.. (keys of S^T, then d of O^T).
+// Softmax warps: two groups of four; group grp owns packed rows
+// [grp*RG, (grp+1)*RG) with RG = NM/2, and warp quarter i of a group reads
+// TMEM lanes 32i.. (keys of S^T, then d of O^T) of the group's columns.  The
+// groups never synchronise with each other: every row's running state lives
+// in one group.
 //
 // Scores stay in S units (the raw QK^T accumulator); c = log2(e) * scale turns
 // them into the log2 domain inside one FFMA.  Per row r the group keeps a
 // reference max m_r (log2 units; kNoMax before any visible key).  One pass per
-// 16-row chunk of a tile: x = S*c - m_r; a vote of the four warps (a named
-// barrier) checks x <= tau for every visible score, and then P = 2^x is
-// written as FP16 (at most 2^tau) with no cross-lane reduction.  A chunk whose
-// vote fails takes the row maxima of the tile, moves the references, rescales
-// the row sums and the O^T columns of those rows, and recomputes x.  Each
-// thread keeps the running row sums of its own key slot for all rows and the
-// group reduces them once per item.  Every wait is bounded; a wait that runs
-// out is reported through the next vote, so the four warps always leave
+// tile over the group's rows: x = S*c - m_r; a vote of the group's four warps
+// (a named barrier) checks x <= tau for every visible score, and then P = 2^x
+// is written as FP16 (at most 2^tau) with no cross-lane reduction.  A tile
+// whose vote fails takes the row maxima of the tile, moves the references,
+// rescales the row sums and the O^T columns of those rows, and recomputes x.
+// Each thread keeps the running row sums of its own key slot for the group's
+// rows, reduced once per item.  Every wait is bounded; a wait that runs out
+// is reported through the next vote, so the group's warps always leave
 // together and never strand one another at a barrier.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb,
+__device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int grp, int i, int lane, uint32_t tb,
                                              uint8_t* pbuf) {
-  using BF = Butterfly<NM, 16>;
-  using BF16R = Butterfly<16, 16>;
+  constexpr int RG = NM / 2;  // rows of the group, a multiple of 8
+  using BF = Butterfly<RG, 16>;
   constexpr int CNT = BF::Count;
   constexpr int kHalves = Fmt::D / 128;
   WaitCtl* abort = &M.ctl;
-  const int gt = 32 * i + lane;  // thread index inside the softmax group
+  const int gt = 32 * i + lane;  // thread index inside the group = key of the tile
+  const int row0 = grp * RG;
+  const int bar_id = kSoftmaxBar + grp;
   const float c_log2 = Fmt::score_scale(a.k_scale);
   const uint32_t lane_base = tb + ((uint32_t)(32 * i) << 16);
-  const int rbase = BF::base(lane);  // rows rbase .. rbase+CNT-1 of every butterfly result
+  const int rbase = BF::base(lane);  // rows row0+rbase .. +CNT-1 of every butterfly result
   uint32_t j = 0, nvote = 0;
   bool bad = false;
   // returns bit 0: some warp saw an exceeding score, bit 1: some wait ran out
   auto vote = [&](bool ex) -> int {
     const int f = (__any_sync(0xffffffffu, ex) ? 1 : 0) | (__any_sync(0xffffffffu, bad) ? 2 : 0);
-    int* slot = M.vote[nvote & 1];
+    int* slot = M.vote[grp][nvote & 1];
     ++nvote;
     if (lane == 0) slot[i] = f;
-    named_bar_sync(kSoftmaxBar, 128);
+    named_bar_sync(bar_id, 128);
     const int4 w = *reinterpret_cast<const int4*>(slot);
     return w.x | w.y | w.z | w.w;
+  };
+  // RG consecutive TMEM columns of this thread's lane
+  auto tmem_load_rows = [&](uint32_t addr, uint32_t (&r)[RG]) {
+#pragma unroll
+    for (int c = 0; c < RG / 8; ++c) PA_TMEM_LD_X8(addr + 8 * c, r + 8 * c);
+    tmem_wait_ld();
+    reg_fence(r);
   };
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
     const int lim = x.L - a.q_len;  // packed row r sees key t iff t <= lim + r / G
-    float lsum[NM];                 // running row sums of this thread's key slot
+    float lsum[RG];                 // running row sums of this thread's key slot
 #pragma unroll
-    for (int r = 0; r < NM; ++r) lsum[r] = 0.f;
+    for (int r = 0; r < RG; ++r) lsum[r] = 0.f;
     for (int jl = 0; jl < nt; ++jl, ++j) {
       bad |= !mbar_wait(&M.s_full[j & 1], (j >> 1) & 1, abort);
       // P^T buffer j % kPBufs is free once PV(j - kPBufs) is done
       const uint32_t pb = j % kPBufs;
       if (j >= kPBufs) bad |= !mbar_wait(&M.pv_done[pb], ((j / kPBufs) - 1) & 1, abort);
       tc_fence_after();
-      const uint32_t s_addr = lane_base + kColS + (j & 1) * 64;
+      const uint32_t s_addr = lane_base + kColS + (j & 1) * 64 + row0;
       const int tile0 = x.t0 + jl * kTileKeys;
       const int key = tile0 + gt;
       const int vis_end = min(x.t1, lim + 1);  // keys below this are visible to every row
       const bool masked_tile = tile0 + kTileKeys > vis_end || NM > a.R;
       uint8_t* prow = pbuf + pb * 16384 + gt * 128;
-      // 16 scores of rows 16*c16.. from TMEM, masked to -inf where invisible
-      auto load_scores = [&](int c16, float (&v)[16]) {
-        uint32_t r[16];
-        tmem_load16(s_addr + 16 * c16, r);
+      // the group's scores of this key, masked to -inf where invisible
+      auto load_scores = [&](float (&v)[RG]) {
+        uint32_t r[RG];
+        tmem_load_rows(s_addr, r);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+        for (int k = 0; k < RG; ++k) v[k] = __uint_as_float(r[k]);
         if (masked_tile) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int row = 16 * c16 + k;
+          for (int k = 0; k < RG; ++k) {
+            const int row = row0 + k;
             const bool vis = (row < a.R) && (key < x.t1) && (key <= lim + row / a.G);
             if (!vis) v[k] = -INFINITY;
           }
         }
       };
+      // v becomes x = S*c - m_ref (log2 units)
+      auto to_log2 = [&](float (&v)[RG]) {
 #pragma unroll
-      for (int c16 = 0; c16 < NM / 16; ++c16) {
-        float v[16];
-        load_scores(c16, v);
-        float mr[16];  // the chunk's reference maxima
-#pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-          const float4 m = *reinterpret_cast<const float4*>(&M.mref[16 * c16 + k]);
-          mr[k] = m.x, mr[k + 1] = m.y, mr[k + 2] = m.z, mr[k + 3] = m.w;
+        for (int k = 0; k < RG; k += 4) {
+          const float4 m = *reinterpret_cast<const float4*>(&M.mref[row0 + k]);
+          v[k] = fmaf(v[k], c_log2, -m.x);
+          v[k + 1] = fmaf(v[k + 1], c_log2, -m.y);
+          v[k + 2] = fmaf(v[k + 2], c_log2, -m.z);
+          v[k + 3] = fmaf(v[k + 3], c_log2, -m.w);
         }
-        bool ex = false;
+      };
+      float v[RG];
+      load_scores(v);
+      to_log2(v);
+      bool ex = false;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) ex |= fmaf(v[k], c_log2, -mr[k]) > kTau;
-        const int f = vote(ex);
-        if (f & 2) return;
-        if (f & 1) {
-          // tile max of the chunk's rows: a 16-row butterfly leaves one row per lane
-          float mx[BF16R::Half];
-          BF16R::template run_from<true>(v, mx, lane);
-          M.red[i][16 * c16 + BF16R::base(lane)] = mx[0];
-          named_bar_sync(kSoftmaxBar, 128);
-          if (gt < 16) {
-            const int row = 16 * c16 + gt;
-            const float m_old = M.mref[row];
-            const float tmax = fmaxf(fmaxf(M.red[0][row], M.red[1][row]), fmaxf(M.red[2][row], M.red[3][row]));
-            const float m_new = fmaxf(m_old, tmax * c_log2);  // tmax = -inf keeps m_old
-            M.mref[row] = m_new;
-            M.alpha[gt] = (m_new == m_old) ? 1.0f : exp2f(m_old - m_new);
-          }
-          named_bar_sync(kSoftmaxBar, 128);
-          bool resc = false;
+      for (int k = 0; k < RG; ++k) ex |= v[k] > kTau;
+      const int f = vote(ex);
+      if (f & 2) return;
+      if (f & 1) {
+        // tile max of the group's rows from the raw scores (reloaded)
+        load_scores(v);
+        float mx[BF::Half];
+        BF::template run_from<true>(v, mx, lane);
 #pragma unroll
-          for (int k = 0; k < 16; k += 4) {
-            const float4 al = *reinterpret_cast<const float4*>(&M.alpha[k]);
-            lsum[16 * c16 + k] *= al.x, lsum[16 * c16 + k + 1] *= al.y;
-            lsum[16 * c16 + k + 2] *= al.z, lsum[16 * c16 + k + 3] *= al.w;
-            resc |= (al.x != 1.0f) | (al.y != 1.0f) | (al.z != 1.0f) | (al.w != 1.0f);
-          }
-          if (resc && jl > 0) {
-            // O^T holds tiles < j of this item: wait for PV(j-1), then scale
-            // columns 16*c16.. (rows of this chunk) by alpha
-            bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
-            tc_fence_after();
+        for (int k = 0; k < CNT; ++k) M.red[i][row0 + rbase + k] = mx[k];
+        named_bar_sync(bar_id, 128);
+        if (gt < RG) {
+          const int row = row0 + gt;
+          const float m_old = M.mref[row];
+          const float tmax = fmaxf(fmaxf(M.red[0][row], M.red[1][row]), fmaxf(M.red[2][row], M.red[3][row]));
+          const float m_new = fmaxf(m_old, tmax * c_log2);  // tmax = -inf keeps m_old
+          M.mref[row] = m_new;
+          M.alpha[row] = (m_new == m_old) ? 1.0f : exp2f(m_old - m_new);
+        }
+        named_bar_sync(bar_id, 128);
+        bool resc = false;
 #pragma unroll
-            for (int h = 0; h < kHalves; ++h) {
-              uint32_t r[16];
-              const uint32_t ta = lane_base + kColO + 64 * h + 16 * c16;
-              tmem_load16(ta, r);
+        for (int k = 0; k < RG; k += 4) {
+          const float4 al = *reinterpret_cast<const float4*>(&M.alpha[row0 + k]);
+          lsum[k] *= al.x, lsum[k + 1] *= al.y, lsum[k + 2] *= al.z, lsum[k + 3] *= al.w;
+          resc |= (al.x != 1.0f) | (al.y != 1.0f) | (al.z != 1.0f) | (al.w != 1.0f);
+        }
+        if (resc && jl > 0) {
+          // O^T holds tiles < j of this item: wait for PV(j-1), then scale
+          // the group's columns (rows) by alpha
+          bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
+          tc_fence_after();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * M.alpha[k]);
-              PA_TMEM_ST_X16(ta, r);
+          for (int h = 0; h < kHalves; ++h) {
+#pragma unroll
+            for (int c = 0; c < RG / 8; ++c) {
+              uint32_t r[8];
+              const uint32_t ta = lane_base + kColO + 64 * h + row0 + 8 * c;
+              PA_TMEM_LD_X8(ta, r);
+              tmem_wait_ld();
+              reg_fence(r);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * M.alpha[row0 + 8 * c + k]);
+              PA_TMEM_ST_X8(ta, r);
             }
-            tmem_wait_st();
           }
-          load_scores(c16, v);  // reloaded rather than held across the rescale
-#pragma unroll
-          for (int k = 0; k < 16; k += 4) {
-            const float4 m = *reinterpret_cast<const float4*>(&M.mref[16 * c16 + k]);
-            mr[k] = m.x, mr[k + 1] = m.y, mr[k + 2] = m.z, mr[k + 3] = m.w;
-          }
+          tmem_wait_st();
         }
-        // probabilities with the (possibly moved) references -> the P^T row
-        // of this key (MN-major: one 128-byte row per key, 8-row pieces
-        // swizzled).  A masked score is -inf, so its probability is exactly 0.
-#pragma unroll
-        for (int h8 = 0; h8 < 2; ++h8) {
-          const int c8 = 2 * c16 + h8;
-          float p[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) p[k] = ex2_approx(fmaf(v[8 * h8 + k], c_log2, -mr[8 * h8 + k]));
-          __half2 h0 = __floats2half2_rn(p[0], p[1]);
-          __half2 h1 = __floats2half2_rn(p[2], p[3]);
-          __half2 h2 = __floats2half2_rn(p[4], p[5]);
-          __half2 h3 = __floats2half2_rn(p[6], p[7]);
-          uint4 w;
-          w.x = *reinterpret_cast<uint32_t*>(&h0);
-          w.y = *reinterpret_cast<uint32_t*>(&h1);
-          w.z = *reinterpret_cast<uint32_t*>(&h2);
-          w.w = *reinterpret_cast<uint32_t*>(&h3);
-          *reinterpret_cast<uint4*>(prow + ((c8 ^ (gt & 7)) << 4)) = w;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) lsum[8 * c8 + k] += p[k];
-        }
+        load_scores(v);  // reloaded rather than held across the rescale
+        to_log2(v);
       }
-      // P^T buffer pb complete and any O^T rescale of this tile stored; S[j&1]
-      // was read for the last time, so QK(j+2) may overwrite it
+      // probabilities with the (possibly moved) references -> the P^T row
+      // of this key (MN-major: one 128-byte row per key, 8-row pieces
+      // swizzled).  A masked score is -inf, so its probability is exactly 0.
+#pragma unroll
+      for (int c8 = 0; c8 < RG / 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[k] = ex2_approx(v[8 * c8 + k]);
+        __half2 h0 = __floats2half2_rn(p[0], p[1]);
+        __half2 h1 = __floats2half2_rn(p[2], p[3]);
+        __half2 h2 = __floats2half2_rn(p[4], p[5]);
+        __half2 h3 = __floats2half2_rn(p[6], p[7]);
+        uint4 w;
+        w.x = *reinterpret_cast<uint32_t*>(&h0);
+        w.y = *reinterpret_cast<uint32_t*>(&h1);
+        w.z = *reinterpret_cast<uint32_t*>(&h2);
+        w.w = *reinterpret_cast<uint32_t*>(&h3);
+        const int piece = row0 / 8 + c8;
+        *reinterpret_cast<uint4*>(prow + ((piece ^ (gt & 7)) << 4)) = w;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lsum[8 * c8 + k] += p[k];
+      }
+      // P^T buffer pb complete (this group's rows) and any O^T rescale of this
+      // tile stored; S[j&1] was read for the last time by this group
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.p_full[pb]);
     }
-    // ---- epilogue: (m, l, O) partials of this item
+    // ---- epilogue: (m, l, O) partials of the group's rows of this item
     BF::template run<false>(lsum, lane);
 #pragma unroll
-    for (int k = 0; k < CNT; ++k) M.red[i][rbase + k] = lsum[k];
-    named_bar_sync(kSoftmaxBar, 128);
+    for (int k = 0; k < CNT; ++k) M.red[i][row0 + rbase + k] = lsum[k];
+    named_bar_sync(bar_id, 128);
     const size_t pi = panel_index(a, x);
-    if (gt < a.R) {
-      const float l = (M.red[0][gt] + M.red[1][gt]) + (M.red[2][gt] + M.red[3][gt]);
-      a.panel_ml[pi + gt] = make_float2(l > 0.f ? M.mref[gt] : -INFINITY, l);
+    if (gt < RG && row0 + gt < a.R) {
+      const int row = row0 + gt;
+      const float l = (M.red[0][row] + M.red[1][row]) + (M.red[2][row] + M.red[3][row]);
+      a.panel_ml[pi + row] = make_float2(l > 0.f ? M.mref[row] : -INFINITY, l);
     }
     bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
     tc_fence_after();
 #pragma unroll
     for (int h = 0; h < kHalves; ++h) {
+      uint32_t r[RG];
+      tmem_load_rows(lane_base + kColO + 64 * h + row0, r);
 #pragma unroll
-      for (int c16 = 0; c16 < NM / 16; ++c16) {
-        uint32_t r[16];
-        tmem_load16(lane_base + kColO + 64 * h + 16 * c16, r);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int row = 16 * c16 + k;
-          if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[k]);
-        }
+      for (int k = 0; k < RG; ++k) {
+        const int row = row0 + k;
+        if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[k]);
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&M.o_free);
-    named_bar_sync(kSoftmaxBar, 128);  // every warp is done with mref and red
-    if (gt < kMaxRows) M.mref[gt] = kNoMax;
-    named_bar_sync(kSoftmaxBar, 128);
+    named_bar_sync(bar_id, 128);  // every warp of the group is done with mref and red
+    if (gt < RG) M.mref[row0 + gt] = kNoMax;
+    named_bar_sync(bar_id, 128);
   }
 }
 
@@ -821,16 +838,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
       mbar_init(&M.vtile_full[s], 4);
     }
     for (int s = 0; s < kPBufs; ++s) {
-      mbar_init(&M.p_full[s], 4);
+      mbar_init(&M.p_full[s], 8);  // the eight softmax warps
       mbar_init(&M.pv_done[s], 1);
     }
     mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
-    mbar_init(&M.o_free, 4);
+    mbar_init(&M.o_free, 8);
     mbar_init(&M.fin, 1);
     M.ctl.abort = 0;
     M.ctl.limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
-    for (int w = 0; w < 8; ++w) M.vote[w / 4][w % 4] = 0;
+    for (int w = 0; w < 16; ++w) M.vote[w / 8][(w / 4) & 1][w % 4] = 0;
     mbar_fence_init();
   }
   if (tid < kMaxRows) M.mref[tid] = kNoMax;
@@ -880,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   } else if (vq >= 0) {
     role_vdecode<Fmt, NM>(a, M, vq, lane, sm + L::kOffVst, sm + L::kOffV);
   } else {
-    role_softmax<Fmt, NM>(a, M, warp - 12, lane, tb, sm + L::kOffP);
+    role_softmax<Fmt, NM>(a, M, (warp - 12) / 4, warp & 3, lane, tb, sm + L::kOffP);
   }
 
   tc_fence_before();
