@@ -24,8 +24,9 @@
 //   3  K loader   one thread: TMA (or the warp: cp.async for 8-byte aligned
 //                 data) of block-table-gathered K rows, a tile at a time
 //   9  V loader   the same for V
-//   11 Q loader   the packed Q tile of each item (128-byte swizzle)
-//   1  MMA        one thread issues tcgen05.mma and commits to mbarriers
+//   11 Q + QK     the packed Q tile of each item (128-byte swizzle); one
+//                 thread issues the QK tcgen05.mma products
+//   1  PV         one thread issues the PV tcgen05.mma products
 //   4-7  K decode staging -> K' in TMEM (lane = key), the QK A operand
 //   0, 8, 2, 10  V decode, key quarters 0-3: staging -> V' in a ring of
 //                MN-major SMEM quarter slots
@@ -100,7 +101,7 @@ constexpr uint32_t kColK = 256;   // K' operand, 2 buffers of 128 columns
 struct Misc {
   uint64_t kst_full, kst_empty, vst_full, vst_empty;  // the K and V staging tiles
   uint64_t kbuf_full[2], s_full[2], vtile_full[2], p_full[kPBufs], pv_done[kPBufs];
-  uint64_t q_full, q_empty, o_free, fin;
+  uint64_t q_full, q_empty, o_free, fin, fin_qk;
   uint32_t tmem_base;
   WaitCtl ctl;
   alignas(16) int vote[2][2][4];     // per-warp vote words of each softmax group, double-buffered
@@ -392,31 +393,59 @@ done:
   cp_async_wait_all();
 }
 
-// Q loader: packed row r = qi * G + hl holds query head g*G + hl of verify
-// query qi.  K-major operand: element (r, d) at (d/64)*(NM*128) + r*128 +
-// ((((d%64)/8) ^ (r%8)) * 16) + (d%8)*2.
+// Q tile and QK issuer (one warp): per item the warp loads the packed Q tile
+// (row r = qi * G + hl holds query head g*G + hl of verify query qi; K-major,
+// element (r, d) at (d/64)*(NM*128) + r*128 + ((((d%64)/8) ^ (r%8)) * 16) +
+// (d%8)*2) once every QK of the previous item completed (q_empty); lane 0 then
+// issues QK(j) for the item's tiles (S^T[128 keys x N] = K' Q^T, 16 steps of
+// K = 16, FP32 in TMEM), each once K'(j) is written and S[j&1] is free (the
+// softmax signalled P^T(j-2) after its last read of it), and commits to
+// s_full (which also frees K'[j&1]); an item's last QK also to q_empty.  The
+// PV products come from another thread (role_pv), so that neither stream of
+// tensor-core work waits behind the other's dependencies.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_qload(const SplitArgs& a, Misc& M, int lane, uint8_t* qbuf) {
-  constexpr int kPieces = Fmt::D / 8;  // 16-byte pieces per Q row
+__device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane, uint8_t* qbuf, uint32_t tb) {
+  using L = Layout<Fmt, NM>;
+  constexpr int kPieces = Fmt::D / 8;
+  constexpr uint32_t id_qk = idesc_f16(128, NM, Fmt::kQBf16, 0, 0);
+  constexpr int kKSteps = Fmt::D / 16;
   WaitCtl* abort = &M.ctl;
   const uint16_t* q = reinterpret_cast<const uint16_t*>(a.q);
-  uint32_t n = 0;
-  for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x, ++n) {
+  const uint64_t q_desc = sdesc_sw128(smem_u32(qbuf), 16, 1024);
+  uint32_t j = 0;
+  bool ok = true;
+  for (int it = blockIdx.x, n = 0; ok && it < M.sched.total; it += gridDim.x, ++n) {
     const Item x = sched_item(M.sched, a.B, it);
+    const int nt = tiles_of(x);
     if (!mbar_wait(&M.q_empty, (n & 1) ^ 1, abort)) break;
     for (int u = lane; u < a.R * kPieces; u += 32) {
-      const int r = u / kPieces, c = u % kPieces;  // piece c holds d = 8c .. 8c+7
+      const int r = u / kPieces, c = u % kPieces;
       const int qi = r / a.G, hl = r % a.G;
       const uint16_t* src = q + ((size_t)(x.b * a.q_len + qi) * a.Hq + x.g * a.G + hl) * Fmt::D + c * 8;
       const uint32_t dst = smem_u32(qbuf + (c >> 3) * (NM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
       cp_async_16(dst, src, 16u);
     }
-    // the tensor core reads Q through the async proxy: land the copies, fence,
-    // then signal
     cp_async_wait_all();
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && !a.withhold_q) mbar_arrive(&M.q_full);  // withheld only by the timeout test hook
+    if (lane == 0) {
+      if (!a.withhold_q) mbar_arrive(&M.q_full);  // withheld only by the timeout test hook
+      ok = mbar_wait(&M.q_full, n & 1, abort);
+      for (int jl = 0; ok && jl < nt; ++jl, ++j) {
+        if (j >= 2) ok = mbar_wait(&M.p_full[(j - 2) % kPBufs], ((j - 2) / kPBufs) & 1, abort);
+        ok = ok && mbar_wait(&M.kbuf_full[j & 1], (j >> 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_col = tb + kColS + (j & 1) * 64, k_col = tb + kColK + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk)
+          mma_ts(s_col, k_col + kk * 8, sdesc_add(q_desc, (kk >> 2) * L::kQAtom + (kk & 3) * 32), id_qk,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&M.s_full[j & 1]);
+        if (jl == nt - 1) mma_commit(&M.q_empty);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   }
   cp_async_wait_all();
 }
@@ -527,62 +556,27 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
   }
 }
 
-// MMA issuer (one thread).  It follows the data flow with blocking waits: QK
-// of the first two tiles, then for every tile j, once the softmax has written
-// P^T(j) (which also frees S[j&1]): QK(j+2), then PV(j) once the tile's V'
-// quarters are written (on an item's first tile also after the epilogue
-// released O).  Completion is reported with few commits: QK(j) to s_full
-// (which also frees K'[j&1]), an item's last QK to q_empty, PV(j) to pv_done
-// (which also frees P^T(j) and the V' slots of tile j).  Few waits and
-// commits per tile keep the thread clear of the per-SM shared-memory queues,
-// which the decode warps keep busy.
+// PV issuer (one thread): for every tile j, once the softmax has written
+// P^T(j) and the V decode warps V'(j) (on an item's first tile also once the
+// epilogue released O): O^T[d x N] += V'^T P^T over the tile's four V' slots
+// (2 halves of M 128 x 8 steps of K = 16), committed to pv_done (which also
+// frees P^T(j) and the V' slots of tile j).  Operand descriptors are built
+// once and advanced by compile-time offsets.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_mma(const SplitArgs& a, Misc& M, uint32_t tb, uint32_t qbase, uint32_t pbase,
-                                         uint32_t vbase) {
+__device__ __forceinline__ void role_pv(const SplitArgs& a, Misc& M, uint32_t tb, uint32_t pbase, uint32_t vbase) {
   using L = Layout<Fmt, NM>;
-  constexpr uint32_t id_qk = idesc_f16(128, NM, Fmt::kQBf16, 0, 0);
   constexpr uint32_t id_pv = idesc_f16(128, NM, 0, 1, 1);
-  constexpr int kKSteps = Fmt::D / 16;
   constexpr int kHalves = Fmt::D / 128;
   WaitCtl* abort = &M.ctl;
-  const int total = M.sched.total;
-  // QK cursor: item number qn (item index q_it), local tile q_jl of q_nt, CTA tile qj
-  int qn = 0, q_it = blockIdx.x, q_jl = 0;
-  int q_nt = q_it < total ? tiles_of(sched_item(M.sched, a.B, q_it)) : 0;
-  uint32_t qj = 0;
-  // operand descriptors at offset 0; each MMA adds a compile-time offset
-  const uint64_t q_desc = sdesc_sw128(qbase, 16, 1024);
   const uint64_t v_desc = sdesc_sw128(vbase, L::kVAtom, 1024);
   const uint64_t p_desc = sdesc_sw128(pbase, 16384, 1024);
-  auto issue_qk = [&]() -> bool {  // QK of the cursor's tile, then advance; false on a wait that ran out
-    if (q_jl == 0 && !mbar_wait(&M.q_full, qn & 1, abort)) return false;
-    if (!mbar_wait(&M.kbuf_full[qj & 1], (qj >> 1) & 1, abort)) return false;
-    tc_fence_after();
-    const uint32_t s_col = tb + kColS + (qj & 1) * 64, k_col = tb + kColK + (qj & 1) * 128;
-#pragma unroll
-    for (int kk = 0; kk < kKSteps; ++kk)
-      mma_ts(s_col, k_col + kk * 8, sdesc_add(q_desc, (kk >> 2) * L::kQAtom + (kk & 3) * 32), id_qk, kk > 0 ? 1u : 0u);
-    mma_commit(&M.s_full[qj & 1]);
-    if (q_jl == q_nt - 1) mma_commit(&M.q_empty);
-    ++qj;
-    if (++q_jl == q_nt) {
-      q_jl = 0;
-      ++qn;
-      q_it += gridDim.x;
-      q_nt = q_it < total ? tiles_of(sched_item(M.sched, a.B, q_it)) : 0;
-    }
-    return true;
-  };
-  for (int k = 0; k < 2 && q_it < total; ++k)
-    if (!issue_qk()) return;
   uint32_t pj = 0;
-  int slot0 = 0;  // V' slot of the tile's first quarter: (4 * pj) % kVSlots
-  for (int n = 0, it = blockIdx.x; it < total; ++n, it += gridDim.x) {
+  int slot0 = 0;
+  for (int n = 0, it = blockIdx.x; it < M.sched.total; ++n, it += gridDim.x) {
     const int nt = tiles_of(sched_item(M.sched, a.B, it));
     for (int jl = 0; jl < nt; ++jl, ++pj) {
       const uint32_t pb = pj % kPBufs, pu = pj / kPBufs;
       if (!mbar_wait(&M.p_full[pb], pu & 1, abort)) return;
-      if (q_it < total && !issue_qk()) return;  // S[j&1] was read for the last time before P^T(j) was signalled
       if (jl == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, abort)) return;
       if (!mbar_wait(&M.vtile_full[pj & 1], (pj >> 1) & 1, abort)) return;
       tc_fence_after();
@@ -845,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     mbar_init(&M.q_empty, 1);
     mbar_init(&M.o_free, 8);
     mbar_init(&M.fin, 1);
+    mbar_init(&M.fin_qk, 1);
     M.ctl.abort = 0;
     M.ctl.limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
     for (int w = 0; w < 16; ++w) M.vote[w / 8][(w / 4) & 1][w % 4] = 0;
@@ -881,11 +876,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     }
     __syncwarp();
   } else if (warp == 11) {
-    role_qload<Fmt, NM>(a, M, lane, sm + L::kOffQ);
+    role_q_qk<Fmt, NM>(a, M, lane, sm + L::kOffQ, tb);
+    if (lane == 0) {
+      mma_commit(&M.fin_qk);  // the same drain for the QK products
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&M.fin_qk, 0) && clock64() - t0 < M.ctl.limit) {
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      role_mma<Fmt, NM>(a, M, tb, smem_u32(sm + L::kOffQ), smem_u32(sm + L::kOffP), smem_u32(sm + L::kOffV));
-      // drain: every issued MMA must finish before TMEM is released
+      role_pv<Fmt, NM>(a, M, tb, smem_u32(sm + L::kOffP), smem_u32(sm + L::kOffV));
+      // drain: every PV this thread issued must finish before TMEM is released
       mma_commit(&M.fin);
       const long long t0 = clock64();
       while (!mbar_try_wait(&M.fin, 0) && clock64() - t0 < M.ctl.limit) {
