@@ -88,6 +88,9 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
+// Prefetch of the cache line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // ----------------------------------------------------------------- cp.async --
 // 16-byte global->shared copy; src_bytes == 0 fills zeros without reading.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {

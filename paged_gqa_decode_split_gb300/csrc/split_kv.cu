@@ -428,6 +428,16 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
     cp_async_wait_all();
     fence_proxy_async_smem();
     __syncwarp();
+    // the next item's Q rows into L2, so that its Q tile is not a round trip
+    // to HBM at the item boundary (each row is D * 2 bytes of one query head)
+    if (it + (int)gridDim.x < M.sched.total) {
+      const Item y = sched_item(M.sched, a.B, it + gridDim.x);
+      for (int u = lane; u < a.R * (Fmt::D * 2 / 128); u += 32) {
+        const int r = u / (Fmt::D * 2 / 128), l = u % (Fmt::D * 2 / 128);
+        const int qi = r / a.G, hl = r % a.G;
+        prefetch_l2(q + ((size_t)(y.b * a.q_len + qi) * a.Hq + y.g * a.G + hl) * Fmt::D + l * 64);
+      }
+    }
     if (lane == 0) {
       if (!a.withhold_q) mbar_arrive(&M.q_full);  // withheld only by the timeout test hook
       ok = mbar_wait(&M.q_full, n & 1, abort);
