@@ -48,6 +48,11 @@ SMALL = [
     ("fp8_g4_q4", "fp8", [640, 11], dict(group=4, q_len=4)),
     ("fp8_short_contexts", "fp8", [1, 2, 7, 8, 9, 16, 0], {}),
     ("fp8_page48_many_splits", "fp8", [20000, 4097], dict(page_size=48)),
+    # TMA boxes of 64 + 16 slots per page piece, whole 128-slot boxes, and an
+    # interleaved K/V layout that is 16-byte aligned (so loaded by TMA)
+    ("fp8_page80_tma", "fp8", [1000, 333], dict(page_size=80)),
+    ("fp8_page128_tma", "fp8", [2000, 129], dict(page_size=128)),
+    ("fp8_interleaved_16B_tma", "fp8", [900, 257], dict(Hkv=2, page_size=64, layout="interleaved")),
     ("fp8_padded_nan", "fp8", [900, 0, 33, 0], dict(padded=(3,))),
     ("bf16_d128", "bf16", [1500, 2048, 17], dict(Hkv=8, group=4, q_len=1)),
     ("bf16_d128_q4_8B", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="interleaved", base_pad=8)),
