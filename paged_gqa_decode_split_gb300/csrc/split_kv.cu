@@ -464,7 +464,7 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
 // tile; lane = key, column c holds elements d = 2c, 2c+1.
 template <class Fmt>
 __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb,
-                                             const uint8_t* ring) {
+                                             const uint8_t* stage) {
   WaitCtl* abort = &M.ctl;
   uint32_t j = 0;
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
@@ -475,7 +475,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
       // take this key's 256-byte row into registers and hand the stage back
       // at once, so the loader's refill does not wait for the tensor core
       uint4 raw[16];
-      load_stage_row(ring, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
+      load_stage_row(stage, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.kst_empty);
       // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
@@ -516,7 +516,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
 // the PV of the tile that read its previous quarter has completed; the four
 // warps signal the tile's quarters on one barrier.
 template <class Fmt, int NM>
-__device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i, int lane, const uint8_t* ring,
+__device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i, int lane, const uint8_t* stage,
                                              uint8_t* vring) {
   using L = Layout<Fmt, NM>;
   WaitCtl* abort = &M.ctl;
@@ -530,7 +530,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
       if (!mbar_wait(&M.vst_full, j & 1, abort)) return;
       // row into registers, stage back to the loader, then wait for the slot
       uint4 raw[16];
-      load_stage_row(ring, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
+      load_stage_row(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.vst_empty);
       const int slot = (int)(c % L::kVSlots);
@@ -875,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   // warp w runs on sub-partition w % 4; the TMEM lane quarter of the K decode
   // and softmax warps is w % 4 as well.  The V decode warps, the heaviest
   // users of the shared-memory queues, sit on sub-partitions 0 and 2, away
-  // from the MMA issuer on sub-partition 1.
+  // from the PV issuer (sub-partition 1) and the QK issuer (sub-partition 3).
   const int vq = warp == 0 ? 0 : warp == 8 ? 1 : warp == 2 ? 2 : warp == 10 ? 3 : -1;
   if (warp == 3 || warp == 9) {
     const bool is_v = warp == 9;
