@@ -74,13 +74,13 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic():
+def _traffic(workload: str):
     """DRAM bytes per split-kernel launch from the committed ncu capture, or
     None when absent or taken on a different kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        if t.get("kernel_source_hash") != kernel_source_hash():
+        if t.get("kernel_source_hash") != kernel_source_hash() or t.get("workload") != workload:
             return None
         return float(t["dram_bytes_per_launch_full"])
     except Exception:
@@ -194,8 +194,13 @@ def cpu_baseline_sample(w_cpu, seconds_target=15.0):
 def describe(spec) -> str:
     return (f"B{spec.batch} x {spec.max_ctx_len}-token contexts, page {spec.page_size}, Hkv {spec.num_kv_heads}, "
             f"Hq {spec.num_q_heads} (GQA {spec.num_q_heads // spec.num_kv_heads}), q_len {spec.q_len}, "
-            f"D {spec.head_dim}, " + ("FP16 Q, E4M3 K/V per-tensor scales" if spec.kind == "fp8" else "BF16 Q/K/V")
-            + ", random block table")
+            f"D {spec.head_dim}, " + KIND_TEXT[spec.kind] + ", random block table")
+
+
+KIND_TEXT = {"fp8": "FP16 Q, E4M3 K/V per-tensor scales", "e5m2": "FP16 Q, E5M2 K/V per-tensor scales",
+             "bf16": "BF16 Q/K/V"}
+DTYPE_TEXT = {"fp8": "f16xe4m3->f32", "e5m2": "f16xe5m2->f32", "bf16": "bf16->f32"}
+ENTRY_POINT = {"fp8": "pa_decode_fp8", "e5m2": "pa_decode_e5m2", "bf16": "pa_decode_bf16_d128"}
 
 
 def reduce_max(values, dist):
@@ -359,7 +364,11 @@ def run_gpu(args, dist, rank, world, local):
     value = total_bytes / (ms / 1e3) / 1e9
     split_avg_s = split_ms / max(split_n, 1) / 1e3
     achieved = unique / split_avg_s / 1e9
-    traffic = _traffic()
+    traffic = _traffic(name)
+    rotated = unique * nsets
+    l2_note = (f"no flush: every step's KV ({unique / 1e6:.0f} MB) exceeds the 129 MB L2" if unique > 129e6 else
+               f"no flush: {nsets} working sets of {unique / 1e6:.1f} MB rotated per call "
+               f"({rotated / 1e6:.0f} MB in all)" + ("" if rotated > 129e6 else ", L2-resident: latency only"))
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(host)
@@ -367,16 +376,16 @@ def run_gpu(args, dist, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "us_per_call": ms / args.steps * 1e3,
         "pct_of_hbm_peak": 100.0 * value / world / peak,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xe4m3->f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TEXT[spec.kind],
         "data": "synthetic",
         "config": {"workload": describe(spec),
                    "global_batch": spec.batch * world, "seq_len": spec.max_ctx_len,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "working_sets": nsets, "l2": "no flush: every step's KV (537 MB) exceeds the 129 MB L2",
+                   "working_sets": nsets, "l2": l2_note,
                    "unique_kv_bytes_per_call": unique},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "split-KV kernel (pa_decode_fp8 main kernel)",
+                     "kernel": f"split-KV kernel ({ENTRY_POINT[spec.kind]} main kernel)",
                      "kernel_avg_us": split_avg_s * 1e6, "combine_avg_us": comb_ms / max(comb_n, 1) * 1e3,
                      "timed_launches": split_n},
         "gpu_launches": 2 * args.steps,

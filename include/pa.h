@@ -7,14 +7,14 @@
  * buffer; the library allocates no device memory, keeps no per-call state
  * (it caches only the SM count of each device it has launched on), never
  * synchronises inside a decode call, and may be called from several host
- * threads at once.  Both decode calls are stream-ordered and can be captured
+ * threads at once.  The decode calls are stream-ordered and can be captured
  * in a CUDA graph: every launch parameter is passed by value, so a graph never
  * refers to host memory that a later call could overwrite ("SM70 attention and
  * quantized projection coverage across TP sizes", section "Graph replay and
  * long-prefill follow-up": symbol values as kernel arguments, no captured
  * host stack addresses).
  *
- * Operation (both variants).  For request b < batch, verify query
+ * Operation (every variant).  For request b < batch, verify query
  * qi < q_len and query head h < num_q_heads, with G = num_q_heads /
  * num_kv_heads, KV head g = h / G and L = ctx_lens[b]:
  *
@@ -94,7 +94,7 @@ typedef struct pa_caps {
   int32_t page_multiple; /* page_size must be a positive multiple of this */
   int32_t max_ctx;       /* largest max_ctx_len */
   int32_t accum_bits;    /* width of the QK and PV accumulators: 32 */
-  int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8: 256 */
+  int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8 and pa_decode_e5m2: 256 */
   int32_t bf16_head_dim; /* head_dim of pa_decode_bf16_d128: 128 */
   int32_t max_splits;    /* most splits one request is cut into (pa_split_plan's *num_splits) */
   int32_t reserved[6];
@@ -105,7 +105,7 @@ typedef struct pa_params {
   int32_t batch;             /* request slots B, 1 .. max_batch (padded slots have ctx_lens 0) */
   int32_t num_kv_heads;      /* Hkv >= 1 */
   int32_t num_q_heads;       /* Hq = G * Hkv, 1 <= G <= max_group */
-  int32_t head_dim;          /* D: 256 for pa_decode_fp8, 128 for pa_decode_bf16_d128 */
+  int32_t head_dim;          /* D: 256 for pa_decode_fp8 / pa_decode_e5m2, 128 for pa_decode_bf16_d128 */
   int32_t q_len;             /* verify queries per request, 1 .. max_q_len (bf16: 1 .. max_q_len too) */
   int32_t page_size;         /* tokens per page, a positive multiple of page_multiple */
   int32_t max_pages_per_req; /* block_table row length; >= ceil(max_ctx_len / page_size) */
@@ -192,6 +192,25 @@ int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const 
 int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                           const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
                           const float* v_scale, void* out, void* stream);
+
+/* ---- FP16 Q x E5M2 K/V, head_dim 256 ---------------------------------------
+ *
+ * The same decode for a cache stored as E5M2 (1 sign bit, 5 exponent bits
+ * with bias 15, 2 mantissa bits; the OCP 8-bit floating point E5M2 format).
+ * E5M2 KV is one of the cache types that keeps its own graph set beside the
+ * E4M3 one ("DFlash2 concurrent long-context attention", section "Why the
+ * single-request optimization was missing from concurrent decode"), and the
+ * E5M2 graphs are checked against an FP64 reference as well ("SM70 attention
+ * and quantized projection coverage across TP sizes", section "Additional
+ * findings").  Arguments, layouts, alignment, workspace
+ * (pa_decode_fp8_workspace_bytes), errors and results are those of
+ * pa_decode_fp8, with one difference: a K element is E5M2(byte) * *k_scale
+ * and a V element E5M2(byte) * *v_scale.  Codes with an all-ones exponent
+ * (infinities and NaNs) are outside the contract: they propagate through the
+ * arithmetic and the affected rows are undefined. */
+int pa_decode_e5m2(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
+                   const float* v_scale, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- BF16 Q/K/V, head_dim 128 ----------------------------------------------
  *

@@ -18,6 +18,9 @@ Sources followed (see the C file for the full statement of the definition):
     section "Scope" (FP32 or better accumulation for QK and PV).
   * "perf(fa2): port decode GQA group-swap into d128 varlen launcher" (vllm.cpp
     pull request #48), description: the BF16 head-dim-128 decode variant.
+  * E5M2 K/V, a cache type the first page names beside E4M3 (same section as
+    above) and whose graphs "SM70 attention and quantized projection coverage
+    across TP sizes", section "Additional findings", checks against FP64.
 """
 from __future__ import annotations
 
@@ -58,6 +61,8 @@ def _setup(lib: ctypes.CDLL) -> ctypes.CDLL:
     i32, i64, f32, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_e5m2_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_value.restype = ctypes.c_double
     lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_value.restype = ctypes.c_double
     lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
@@ -65,6 +70,8 @@ def _setup(lib: ctypes.CDLL) -> ctypes.CDLL:
     common = [i32] * 7 + [vp, vp, vp] + [i64] * 6 + [vp, vp]
     lib.oracle_paged_attn_fp8.argtypes = common + [f32, f32, vp, i32, vp, vp, i32]
     lib.oracle_paged_attn_fp8.restype = i32
+    lib.oracle_paged_attn_e5m2.argtypes = common + [f32, f32, vp, i32, vp, vp, i32]
+    lib.oracle_paged_attn_e5m2.restype = i32
     lib.oracle_paged_attn_bf16.argtypes = common + [vp, i32, vp, vp, i32]
     lib.oracle_paged_attn_bf16.restype = i32
     lib.oracle_max_threads.restype = i32
@@ -90,6 +97,12 @@ def e4m3_value(codes, lib=None) -> np.ndarray:
     return np.array([lib.oracle_e4m3_value(int(x)) for x in c], dtype=np.float64)
 
 
+def e5m2_value(codes, lib=None) -> np.ndarray:
+    lib = lib or load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e5m2_value(int(x)) for x in c], dtype=np.float64)
+
+
 def f16_value(bits, lib=None) -> np.ndarray:
     lib = lib or load()
     c = np.asarray(bits, dtype=np.uint16).ravel()
@@ -112,7 +125,8 @@ def paged_attn(kind: str, *, q: np.ndarray, kv: np.ndarray, k_offset: int, v_off
                k_scale: float = 1.0, v_scale: float = 1.0, rows=None, num_threads: int = 0, lib=None):
     """Evaluate the definition for every (or the selected) output rows.
 
-    kind          "fp8" (FP16 Q, E4M3 K/V + FP32 scales) or "bf16" (BF16 Q/K/V).
+    kind          "fp8" (FP16 Q, E4M3 K/V + FP32 scales), "e5m2" (FP16 Q, E5M2
+                  K/V + FP32 scales) or "bf16" (BF16 Q/K/V).
     q             uint16 bit patterns [B, q_len, Hq, D].
     kv            one uint8 host buffer holding both K and V pages; K element
                   (page, slot, head, d) is at byte k_offset + page*k_strides[0]
@@ -141,9 +155,9 @@ def paged_attn(kind: str, *, q: np.ndarray, kv: np.ndarray, k_offset: int, v_off
     base = _ptr(kv)
     args = [B, q_len, Hq, num_kv_heads, D, page_size, bt.shape[1], _ptr(q), base + k_offset, base + v_offset,
             *[int(s) for s in k_strides], *[int(s) for s in v_strides], _ptr(bt), _ptr(cl)]
-    if kind == "fp8":
-        rc = lib.oracle_paged_attn_fp8(*args, float(k_scale), float(v_scale), rows_ptr, n_rows, _ptr(out),
-                                       _ptr(lse), int(num_threads))
+    if kind in ("fp8", "e5m2"):
+        fn = lib.oracle_paged_attn_fp8 if kind == "fp8" else lib.oracle_paged_attn_e5m2
+        rc = fn(*args, float(k_scale), float(v_scale), rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
     elif kind == "bf16":
         rc = lib.oracle_paged_attn_bf16(*args, rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
     else:

@@ -22,7 +22,9 @@
  *   key j  -> page block_table[b][j / page_size], slot j % page_size
  *   k_j    = E4M3(K bytes) * k_scale, v_j = E4M3(V bytes) * v_scale, one FP32
  *            scale per tensor (same section: E4M3 KV, FP16 queries, D = 256 is
- *            the kernel's numerical and shape contract).
+ *            the kernel's numerical and shape contract).  An E5M2 cache (a KV
+ *            type the same section names beside E4M3) is read the same way
+ *            with the E5M2 decoder.
  *   s_j    = (q . k_j) / sqrt(D)
  *   out    = sum_j exp(s_j - max s) v_j / sum_j exp(s_j - max s)
  *   lse    = max s + log(sum_j exp(s_j - max s))
@@ -46,6 +48,9 @@
  *   E4M3 (OCP 8-bit floating point specification, E4M3 variant): 1 sign bit,
  *     4 exponent bits with bias 7, 3 mantissa bits, no infinities, the two
  *     codes S.1111.111 are NaN; exponent field 0 is subnormal 2^-6 * m/8.
+ *   E5M2 (same specification, E5M2 variant): 1 sign bit, 5 exponent bits with
+ *     bias 15, 2 mantissa bits; exponent field 31 is infinity (m = 0) or NaN;
+ *     exponent field 0 is subnormal 2^-14 * m/4.
  *   binary16 (IEEE 754): 1 sign, 5 exponent bits with bias 15, 10 mantissa.
  *   bfloat16: the upper 16 bits of an IEEE binary32.
  *
@@ -90,6 +95,31 @@ double oracle_e4m3_value(uint8_t code) {
   return sign ? -mag : mag;
 }
 
+double oracle_e5m2_value(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 2) & 0x1F;
+  int m = code & 0x3;
+  double mag;
+#if ORACLE_MUTATION == 11
+  const int bias = 16;
+#else
+  const int bias = 15;
+#endif
+  if (e == 0x1F) {
+    if (m != 0) return NAN;
+    mag = INFINITY;
+  } else if (e == 0) {
+#if ORACLE_MUTATION == 12
+    mag = ldexp(1.0 + m / 4.0, 1 - bias);
+#else
+    mag = ldexp(m / 4.0, 1 - bias); /* subnormal: 2^(1-bias) * m/4 */
+#endif
+  } else {
+    mag = ldexp(1.0 + m / 4.0, e - bias);
+  }
+  return sign ? -mag : mag;
+}
+
 double oracle_f16_value(uint16_t bits) {
   int sign = (bits >> 15) & 1;
   int e = (bits >> 10) & 0x1F;
@@ -120,6 +150,8 @@ double oracle_bf16_value(uint16_t bits) {
 
 /* ---- one output row ------------------------------------------------------- */
 
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_E5M2 = 2 };
+
 typedef struct {
   int B, q_len, Hq, Hkv, D, page_size, max_pages_per_req;
   const uint16_t* q;      /* [B][q_len][Hq][D], FP16 or BF16 bits */
@@ -130,7 +162,7 @@ typedef struct {
   const int32_t* block_table; /* [B][max_pages_per_req] */
   const int32_t* ctx_lens;    /* [B] */
   double k_scale, v_scale;    /* 1.0 for BF16 K/V */
-  int kv_is_fp8;              /* 1: E4M3 bytes, 0: BF16 elements */
+  int kv_format;              /* KV_BF16, KV_E4M3 or KV_E5M2 */
   int q_is_bf16;              /* 0: FP16 Q, 1: BF16 Q */
 } problem_t;
 
@@ -139,7 +171,8 @@ static double load_q(const problem_t* P, size_t idx) {
 }
 
 static double load_kv(const problem_t* P, const uint8_t* row, int d, double scale) {
-  if (P->kv_is_fp8) return oracle_e4m3_value(row[d]) * scale;
+  if (P->kv_format == KV_E4M3) return oracle_e4m3_value(row[d]) * scale;
+  if (P->kv_format == KV_E5M2) return oracle_e5m2_value(row[d]) * scale;
   uint16_t bits;
   memcpy(&bits, row + 2 * (size_t)d, 2);
   return oracle_bf16_value(bits);
@@ -272,7 +305,23 @@ int oracle_paged_attn_fp8(int B, int q_len, int Hq, int Hkv, int D, int page_siz
                           const int32_t* rows, int n_rows, double* out, double* lse, int num_threads) {
   problem_t P = {B, q_len, Hq, Hkv, D, page_size, max_pages_per_req, q, k_base, v_base,
                  k_page_stride, k_token_stride, k_head_stride, v_page_stride, v_token_stride, v_head_stride,
-                 block_table, ctx_lens, (double)k_scale, (double)v_scale, 1, 0};
+                 block_table, ctx_lens, (double)k_scale, (double)v_scale, KV_E4M3, 0};
+  return run(&P, rows, n_rows, out, lse, num_threads);
+}
+
+/*
+ * FP16 Q, E5M2 K/V with one FP32 scale per tensor.  Same arguments, row
+ * selection and outputs as oracle_paged_attn_fp8.
+ */
+int oracle_paged_attn_e5m2(int B, int q_len, int Hq, int Hkv, int D, int page_size, int max_pages_per_req,
+                           const uint16_t* q, const uint8_t* k_base, const uint8_t* v_base,
+                           int64_t k_page_stride, int64_t k_token_stride, int64_t k_head_stride,
+                           int64_t v_page_stride, int64_t v_token_stride, int64_t v_head_stride,
+                           const int32_t* block_table, const int32_t* ctx_lens, float k_scale, float v_scale,
+                           const int32_t* rows, int n_rows, double* out, double* lse, int num_threads) {
+  problem_t P = {B, q_len, Hq, Hkv, D, page_size, max_pages_per_req, q, k_base, v_base,
+                 k_page_stride, k_token_stride, k_head_stride, v_page_stride, v_token_stride, v_head_stride,
+                 block_table, ctx_lens, (double)k_scale, (double)v_scale, KV_E5M2, 0};
   return run(&P, rows, n_rows, out, lse, num_threads);
 }
 
@@ -288,7 +337,7 @@ int oracle_paged_attn_bf16(int B, int q_len, int Hq, int Hkv, int D, int page_si
                            const int32_t* rows, int n_rows, double* out, double* lse, int num_threads) {
   problem_t P = {B, q_len, Hq, Hkv, D, page_size, max_pages_per_req, q, k_base, v_base,
                  k_page_stride, k_token_stride, k_head_stride, v_page_stride, v_token_stride, v_head_stride,
-                 block_table, ctx_lens, 1.0, 1.0, 0, 1};
+                 block_table, ctx_lens, 1.0, 1.0, KV_BF16, 1};
   return run(&P, rows, n_rows, out, lse, num_threads);
 }
 

@@ -67,6 +67,7 @@ def load() -> ctypes.CDLL:
             "pa_decode_fp8_workspace_bytes": ([pp], sz),
             "pa_decode_fp8": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_fp8_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "pa_decode_e5m2": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_bf16_d128_workspace_bytes": ([pp], sz),
             "pa_decode_bf16_d128": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_read_status": ([vp, _P(ctypes.c_uint32), vp], ctypes.c_int),
@@ -157,6 +158,13 @@ def pa_decode_fp8(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, k_sc
     return load().pa_decode_fp8(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                 _ptr(ctx_lens), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(workspace),
                                 int(workspace_bytes), _stream(stream))
+
+
+def pa_decode_e5m2(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, workspace,
+                   workspace_bytes: int, stream=None) -> int:
+    return load().pa_decode_e5m2(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                 _ptr(ctx_lens), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
 
 
 def pa_decode_fp8_noalloc(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out,

@@ -149,10 +149,11 @@ void timing_slot(int kind, cudaEvent_t* a, cudaEvent_t* b) {
   T.used[kind]++;
 }
 
-int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
                   void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr,
                   bool clear_status = false) {
+  const bool bf16 = fmt == kKvBf16;
   const int D = bf16 ? 128 : 256;
   int R = 0;
   int st = check_geometry(p, D, &R);
@@ -212,7 +213,7 @@ int decode_common(bool bf16, const pa_params* p, const void* q, const void* k_pa
   cudaEvent_t e0, e1;
   timing_slot(0, &e0, &e1);
   if (e0) cudaEventRecord(e0, stream);
-  if (launch_split(a, bf16, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_split(a, fmt, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (e1) cudaEventRecord(e1, stream);
 
   CombineArgs c;
@@ -304,7 +305,14 @@ size_t pa_decode_bf16_d128_workspace_bytes(const pa_params* p) { return workspac
 int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
                   void* out, void* workspace, size_t workspace_bytes_given, void* stream) {
-  return decode_common(false, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
+  return decode_common(kKvE4m3, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
+                       workspace, workspace_bytes_given, stream);
+}
+
+int pa_decode_e5m2(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
+                   void* out, void* workspace, size_t workspace_bytes_given, void* stream) {
+  return decode_common(kKvE5m2, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
                        workspace, workspace_bytes_given, stream);
 }
 
@@ -320,14 +328,14 @@ int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages
   void* scratch = nullptr;
   const int sst = noalloc_scratch(dev, &scratch);
   if (sst != PA_OK) return sst;
-  return decode_common(false, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
+  return decode_common(kKvE4m3, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
                        scratch, kNoallocScratchBytes, stream, /*clear_status=*/true);
 }
 
 int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                         const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse, void* workspace,
                         size_t workspace_bytes_given, void* stream) {
-  return decode_common(true, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, lse, workspace,
+  return decode_common(kKvBf16, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, lse, workspace,
                        workspace_bytes_given, stream);
 }
 

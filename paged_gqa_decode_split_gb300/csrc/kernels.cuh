@@ -7,7 +7,11 @@
 
 namespace pa {
 
-// Split-KV kernel arguments (both element formats).
+// Element formats of the split kernel: FP16 Q with E4M3 or E5M2 K/V (head_dim
+// 256, FP32 per-tensor scales), or BF16 Q/K/V (head_dim 128).
+enum KvFormat : int { kKvE4m3 = 0, kKvBf16 = 1, kKvE5m2 = 2 };
+
+// Split-KV kernel arguments (every element format).
 struct SplitArgs {
   // 4-D byte views (row byte, KV head, slot, page) of K and V for the TMA
   // loaders, with boxes of 128 bytes x 128, 64, 32 and 16 slots; filled when
@@ -15,14 +19,14 @@ struct SplitArgs {
   CUtensorMap k_maps[4];
   CUtensorMap v_maps[4];
   int use_tma;
-  const void* q;               // FP16 (E4M3 path) or BF16 (BF16 path) [B][q_len][Hq][D]
+  const void* q;               // FP16 (E4M3 / E5M2 paths) or BF16 (BF16 path) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs
   const uint8_t* v;
   const int32_t* block_table;  // [B][mpr]
   const int32_t* ctx_lens;     // [B]
-  const float* k_scale;        // E4M3 path only
+  const float* k_scale;        // E4M3 / E5M2 paths only
   float2* panel_ml;            // (m in log2 units, l) per (item, row)
-  float* panel_o;              // unnormalised O per (item, row, d); E4M3 path: without v_scale
+  float* panel_o;              // unnormalised O per (item, row, d); 8-bit paths: without v_scale
   uint32_t* status;
   uint32_t* bad;
   long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
@@ -38,13 +42,13 @@ struct CombineArgs {
   const uint32_t* bad;
   const float* out_scale_ptr;  // nullable: output is multiplied by *out_scale_ptr * out_scale_mul
   float out_scale_mul;
-  void* out;                   // FP16 (E4M3 path) or BF16 (BF16 path)
+  void* out;                   // FP16 (8-bit K/V paths) or BF16 (BF16 path)
   float* lse;                  // nullable
   int B, Hkv, Hq, G, q_len, R, D, max_ctx, s_max;
 };
 
 int split_smem_bytes();
-cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, cudaStream_t stream);
+cudaError_t launch_split(const SplitArgs& a, KvFormat fmt, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream);
 cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
                                   int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream);

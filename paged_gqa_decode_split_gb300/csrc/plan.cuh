@@ -162,4 +162,14 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32
       : "r"(x));
 }
 
+// ------------------------------------------------------------ E5M2 -> FP16 --
+// E5M2 (1 sign, 5 exponent bits with bias 15, 2 mantissa bits) has the field
+// layout of the upper byte of an IEEE binary16, so code c decodes exactly to
+// the FP16 bit pattern c << 8 (subnormals included).  Same packing as
+// e4m3x4_to_f16x4.
+__device__ __forceinline__ void e5m2x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(x, 0u, 0x1404);  // bytes: 0, code 0, 0, code 1
+  hi = __byte_perm(x, 0u, 0x3424);  // bytes: 0, code 2, 0, code 3
+}
+
 }  // namespace pa

@@ -1,6 +1,7 @@
 // Split-KV paged decode / speculative-verify attention on the sm_103a tensor
-// cores (tcgen05 + TMEM), for two element formats:
+// cores (tcgen05 + TMEM), for three element formats:
 //   Fp8Fmt : FP16 Q, E4M3 K/V with FP32 per-tensor scales, head_dim 256
+//   E5m2Fmt: FP16 Q, E5M2 K/V with FP32 per-tensor scales, head_dim 256
 //   Bf16Fmt: BF16 Q/K/V, head_dim 128
 //
 // One work item = (request b, KV head g, split s) = keys [t0, t1) of request b.
@@ -15,8 +16,8 @@
 //   O^T[d][row]  += V'^T[d][key] P^T[key][row]  A = V' (SMEM, MN-major), B = P (SMEM, MN-major)
 // with FP32 accumulators in TMEM ("SM70 attention and quantized projection
 // coverage across TP sizes", section "Scope": FP16 inputs with FP32
-// accumulation for both QK and PV).  For E4M3, K' and V' are the codes decoded
-// exactly to FP16; for BF16, K' is K and V' is V converted to FP16 so
+// accumulation for both QK and PV).  For E4M3 and E5M2, K' and V' are the
+// codes decoded exactly to FP16; for BF16, K' is K and V' is V converted to FP16 so
 // that P can stay FP16 in the PV product.  Each TMEM lane is one key, so the
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
@@ -63,6 +64,17 @@ struct Fp8Fmt {
     e4m3x4_to_f16x4(x.y, w[2], w[3]);
     e4m3x4_to_f16x4(x.z, w[4], w[5]);
     e4m3x4_to_f16x4(x.w, w[6], w[7]);
+  }
+};
+
+// E5M2 K/V: the geometry, scales and score scale of the E4M3 path; only the
+// decode differs (every finite E5M2 value, |x| <= 57344, is an FP16 value)
+struct E5m2Fmt : Fp8Fmt {
+  static __device__ __forceinline__ void decode16(uint4 x, uint32_t* w) {
+    e5m2x4_to_f16x4(x.x, w[0], w[1]);
+    e5m2x4_to_f16x4(x.y, w[2], w[3]);
+    e5m2x4_to_f16x4(x.z, w[4], w[5]);
+    e5m2x4_to_f16x4(x.w, w[6], w[7]);
   }
 };
 
@@ -956,9 +968,13 @@ cudaError_t launch_mode(const SplitArgs& a, int grid, cudaStream_t stream) {
 
 int split_smem_bytes() { return Layout<Fp8Fmt, 64>::kSmemBytes; }
 
-cudaError_t launch_split(const SplitArgs& a, bool bf16, int grid, cudaStream_t stream) {
-  if (bf16) return a.use_tma ? launch_mode<Bf16Fmt, 1>(a, grid, stream) : launch_mode<Bf16Fmt, 0>(a, grid, stream);
-  return a.use_tma ? launch_mode<Fp8Fmt, 1>(a, grid, stream) : launch_mode<Fp8Fmt, 0>(a, grid, stream);
+cudaError_t launch_split(const SplitArgs& a, KvFormat fmt, int grid, cudaStream_t stream) {
+  switch (fmt) {
+    case kKvE4m3: return a.use_tma ? launch_mode<Fp8Fmt, 1>(a, grid, stream) : launch_mode<Fp8Fmt, 0>(a, grid, stream);
+    case kKvE5m2: return a.use_tma ? launch_mode<E5m2Fmt, 1>(a, grid, stream) : launch_mode<E5m2Fmt, 0>(a, grid, stream);
+    case kKvBf16: return a.use_tma ? launch_mode<Bf16Fmt, 1>(a, grid, stream) : launch_mode<Bf16Fmt, 0>(a, grid, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

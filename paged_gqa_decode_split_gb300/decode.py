@@ -20,7 +20,8 @@ def params_for(w: Workload) -> B.pa_params:
 
 class Decoder:
     """Holds the device-side buffers one workload needs (output, workspace,
-    scales) and enqueues pa_decode_fp8 / pa_decode_bf16_d128 on a stream."""
+    scales) and enqueues pa_decode_fp8 / pa_decode_e5m2 / pa_decode_bf16_d128 on
+    a stream."""
 
     def __init__(self, w: Workload, *, with_lse: bool = False):
         if not w.q.is_cuda:
@@ -29,7 +30,8 @@ class Decoder:
         self.p = params_for(w)
         s = w.spec
         dev = w.q.device
-        self.fp8 = s.kind == "fp8"
+        self.kind = s.kind
+        self.fp8 = s.kind in ("fp8", "e5m2")   # 8-bit K/V with per-tensor scales
         nbytes = (B.pa_decode_fp8_workspace_bytes(self.p) if self.fp8 else
                   B.pa_decode_bf16_d128_workspace_bytes(self.p))
         if nbytes == 0:
@@ -52,9 +54,10 @@ class Decoder:
         w = self.w
         kv = w.kv.data_ptr()
         if self.fp8:
-            return B.pa_decode_fp8(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
-                                   self.scales.data_ptr(), self.scales.data_ptr() + 4, self.out, self.workspace,
-                                   self.ws_bytes, stream)
+            fn = B.pa_decode_fp8 if self.kind == "fp8" else B.pa_decode_e5m2
+            return fn(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
+                      self.scales.data_ptr(), self.scales.data_ptr() + 4, self.out, self.workspace, self.ws_bytes,
+                      stream)
         return B.pa_decode_bf16_d128(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
                                      self.out, self.lse, self.workspace, self.ws_bytes, stream)
 

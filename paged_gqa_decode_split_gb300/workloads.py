@@ -18,7 +18,11 @@ Workload shapes follow the pages' validation and timing fixtures:
 Value recipe: Q ~ N(0, 1) in FP16 (BF16 for d128).  K and V ~ N(0, 1) drawn in
 FP32; for E4M3 each of K and V gets one FP32 scale amax/448 and the bytes are
 clamp(x / scale, -448, 448) cast to E4M3 with round-to-nearest-even by torch's
-float8_e4m3fn conversion.  Pages are assigned to requests through a random
+float8_e4m3fn conversion.  E5M2 K/V (a cache type that keeps its own graph
+set beside E4M3: "DFlash2 concurrent long-context attention", section "Why the
+single-request optimization was missing from concurrent decode") follows the
+same recipe with the format's largest finite value, 57344, in place of 448 and
+torch's float8_e5m2 conversion.  Pages are assigned to requests through a random
 permutation of the pool; block-table entries past a request's last page are -1
 and must never be read.  Padded batch slots have ctx_len 0, Q = NaN and a block
 table row of -1.
@@ -32,6 +36,7 @@ from typing import Optional, Sequence
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 @dataclasses.dataclass(frozen=True)
@@ -39,7 +44,7 @@ class Spec:
     """Shape and structure of one workload (values are drawn by ``generate``)."""
 
     name: str
-    kind: str                      # "fp8": FP16 Q + E4M3 K/V, "bf16": BF16 Q/K/V
+    kind: str                      # "fp8": FP16 Q + E4M3 K/V, "e5m2": FP16 Q + E5M2 K/V, "bf16": BF16 Q/K/V
     batch: int
     num_kv_heads: int
     num_q_heads: int
@@ -57,7 +62,7 @@ class Spec:
 
     @property
     def elem_bytes(self) -> int:
-        return 1 if self.kind == "fp8" else 2
+        return 1 if self.kind in ("fp8", "e5m2") else 2
 
     @property
     def max_pages_per_req(self) -> int:
@@ -98,11 +103,15 @@ SPECS: dict[str, Spec] = {
     "b16_mixed": Spec("b16_mixed", "fp8", 16, 2, 12, 256, 8, 3296, 262144, ctx_range=(0, 262144),
                       zero_slots=(4, 9), padded_slots=(13, 14, 15), layout="interleaved", base_pad=8),
 }
+# E5M2 K/V on the E4M3 configurations' shapes
+for _n in ("b1_l3297", "b8_l128k"):
+    SPECS[_n + "_e5m2"] = dataclasses.replace(SPECS[_n], name=_n + "_e5m2", kind="e5m2")
 for _b in (1, 2, 4, 8):
     SPECS[f"d128_b{_b}"] = Spec(f"d128_b{_b}", "bf16", _b, 8, 32, 128, 1, 16, 32768, ctx_range=(1024, 32768))
 
 CONFIG_SEED = {"b1_l3297": 1000, "b4_l32k": 1001, "b8_l128k": 1002, "b16_mixed": 1003,
-               "d128_b1": 1004, "d128_b2": 1014, "d128_b4": 1024, "d128_b8": 1034}
+               "d128_b1": 1004, "d128_b2": 1014, "d128_b4": 1024, "d128_b8": 1034,
+               "b1_l3297_e5m2": 1005, "b8_l128k_e5m2": 1006}
 
 
 def working_set_seed(name: str, w: int) -> int:
@@ -125,11 +134,13 @@ def _draw_lengths(spec: Spec, gen: torch.Generator) -> list[int]:
     return lens
 
 
-def _quantize_e4m3(x: torch.Tensor) -> tuple[torch.Tensor, float]:
-    """FP32 tensor -> (E4M3 bytes as uint8, FP32 per-tensor scale amax/448)."""
+def _quantize(x: torch.Tensor, kind: str) -> tuple[torch.Tensor, float]:
+    """FP32 tensor -> (8-bit codes as uint8, FP32 per-tensor scale amax/fmax),
+    fmax = 448 for E4M3 ("fp8"), 57344 for E5M2."""
+    fmax, dtype = (E4M3_MAX, torch.float8_e4m3fn) if kind == "fp8" else (E5M2_MAX, torch.float8_e5m2)
     amax = x.abs().max().to(torch.float32)
-    scale = (amax / E4M3_MAX).clamp_min(torch.finfo(torch.float32).tiny)
-    codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    scale = (amax / fmax).clamp_min(torch.finfo(torch.float32).tiny)
+    codes = (x / scale).clamp(-fmax, fmax).to(dtype)
     return codes.view(torch.uint8), float(scale.item())
 
 
@@ -159,18 +170,18 @@ def generate(spec: Spec, seed: int, device: str | torch.device = "cpu",
         bt[b, :n] = perm[off:off + n].to(torch.int32)
         off += n
     # queries
-    qdtype = torch.float16 if spec.kind == "fp8" else torch.bfloat16
+    qdtype = torch.bfloat16 if spec.kind == "bf16" else torch.float16
     q = torch.randn((B, spec.q_len, Hq, D), generator=gen, device=device, dtype=torch.float32).to(qdtype)
     for i in spec.padded_slots:
         q[i] = float("nan")
     # K and V pages, logical shape [num_pages, ps, Hkv, D]
     shape = (num_pages, ps, Hkv, D)
     kx = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
-    if spec.kind == "fp8":
-        kb, k_scale = _quantize_e4m3(kx)
+    if spec.kind in ("fp8", "e5m2"):
+        kb, k_scale = _quantize(kx, spec.kind)
         del kx
         vx = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
-        vb, v_scale = _quantize_e4m3(vx)
+        vb, v_scale = _quantize(vx, spec.kind)
         del vx
     else:
         kb = kx.to(torch.bfloat16).view(torch.uint8).reshape(*shape[:3], D * 2)
@@ -208,6 +219,6 @@ def small_spec(kind: str = "fp8", *, batch: int = 2, num_kv_heads: int = 1, grou
                page_size: int = 16, max_ctx_len: int = 64, layout: str = "separate", base_pad: int = 0,
                head_dim: Optional[int] = None, name: str = "small") -> Spec:
     """A small spec for tests (lengths are passed to ``generate``)."""
-    D = head_dim or (256 if kind == "fp8" else 128)
+    D = head_dim or (128 if kind == "bf16" else 256)
     return Spec(name, kind, batch, num_kv_heads, num_kv_heads * group, D, q_len, page_size, max_ctx_len,
                 ctx_lens=(0,) * batch, layout=layout, base_pad=base_pad)

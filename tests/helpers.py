@@ -25,7 +25,8 @@ def run_oracle(w: wl.Workload, rows=None, lib=None, num_threads: int = 0):
 
 def _elements(w: wl.Workload, which: str, b: int, g: int, n: int) -> torch.Tensor:
     """Dense float64 K or V rows 0..n-1 of request b, KV head g, decoded with
-    torch's own float8_e4m3fn / bfloat16 casts (not the oracle's decoders)."""
+    torch's own float8_e4m3fn / float8_e5m2 / bfloat16 casts (not the oracle's
+    decoders)."""
     s = w.spec
     kv = w.kv.detach().cpu()
     off = w.k_offset if which == "k" else w.v_offset
@@ -40,9 +41,10 @@ def _elements(w: wl.Workload, which: str, b: int, g: int, n: int) -> torch.Tenso
     if not rows:
         return torch.zeros((0, s.head_dim), dtype=torch.float64)
     raw = torch.stack(rows)
-    if s.kind == "fp8":
+    if s.kind in ("fp8", "e5m2"):
         scale = w.k_scale if which == "k" else w.v_scale
-        return raw.view(torch.float8_e4m3fn).to(torch.float64) * torch.tensor(scale, dtype=torch.float32).double()
+        dtype = torch.float8_e4m3fn if s.kind == "fp8" else torch.float8_e5m2
+        return raw.view(dtype).to(torch.float64) * torch.tensor(scale, dtype=torch.float32).double()
     return raw.view(torch.bfloat16).to(torch.float64)
 
 

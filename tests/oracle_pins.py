@@ -6,9 +6,10 @@ deliberately mutated builds (tests/test_oracle_pins.py checks that every planted
 mistake is caught by at least one pin).
 
 What pins what:
-  * element decoders  - every E4M3 / FP16 / BF16 code against torch / numpy casts,
-                        the E4M3 closed form, and the OCP format points in
-                        tests/golden/e4m3_format_points.txt;
+  * element decoders  - every E4M3 / E5M2 / FP16 / BF16 code against torch /
+                        numpy casts, the E4M3 and E5M2 closed forms, and the OCP
+                        format points in tests/golden/e4m3_format_points.txt
+                        and tests/golden/e5m2_format_points.txt;
   * whole definition  - brute force on tiny paged inputs against float64
                         torch.nn.functional.scaled_dot_product_attention with an
                         explicit causal mask (an independent library routine);
@@ -32,6 +33,7 @@ from helpers import dense_reference, run_oracle, visible
 from paged_gqa_decode_split_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e4m3_format_points.txt")
+GOLDEN_E5M2 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e5m2_format_points.txt")
 
 
 def _cmp(name, got, want, atol=0.0, rtol=0.0):
@@ -67,21 +69,49 @@ def pin_e4m3_closed_form(lib):
     return _cmp("e4m3 closed form", oracle.e4m3_value(np.arange(256), lib), want)
 
 
-def pin_e4m3_golden(lib):
+def _golden(path, decode, name):
     codes, vals = [], []
-    for line in open(GOLDEN):
+    for line in open(path):
         line = line.split("#")[0].strip()
         if line:
             c, v = line.split()
             codes.append(int(c, 16))
             vals.append(float(v))
-    got = oracle.e4m3_value(codes, lib)
-    out = _cmp("e4m3 OCP format points", got, vals)
+    got = decode(codes)
+    out = _cmp(f"{name} OCP format points", got, vals)
     # the sign of zero is part of the format
     for c, g in zip(codes, got):
         if c in (0x00, 0x80) and math.copysign(1.0, g) != (-1.0 if c == 0x80 else 1.0):
-            out.append(f"e4m3 code {c:#x} has the wrong zero sign")
+            out.append(f"{name} code {c:#x} has the wrong zero sign")
     return out
+
+
+def pin_e4m3_golden(lib):
+    return _golden(GOLDEN, lambda c: oracle.e4m3_value(c, lib), "e4m3")
+
+
+def pin_e5m2_vs_torch(lib):
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    return _cmp("e5m2 vs torch float8_e5m2", oracle.e5m2_value(codes, lib), want)
+
+
+def pin_e5m2_closed_form(lib):
+    want = []
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 2) & 31, c & 3
+        if e == 31:
+            v = math.inf if m == 0 else math.nan
+        elif e == 0:
+            v = m * 2.0 ** -16                # subnormal: m/4 * 2^-14
+        else:
+            v = (4 + m) * 2.0 ** (e - 17)     # (1 + m/4) * 2^(e-15)
+        want.append(-v if s else v)
+    return _cmp("e5m2 closed form", oracle.e5m2_value(np.arange(256), lib), want)
+
+
+def pin_e5m2_golden(lib):
+    return _golden(GOLDEN_E5M2, lambda c: oracle.e5m2_value(c, lib), "e5m2")
 
 
 def pin_f16_vs_numpy(lib):
@@ -118,6 +148,11 @@ def _bruteforce(lib, kind, **kw):
 def pin_bruteforce_fp8(lib):
     return _bruteforce(lib, "fp8") + _bruteforce(lib, "fp8", Hkv=1, group=6, q_len=8, layout="interleaved",
                                                  base_pad=8)
+
+
+def pin_bruteforce_e5m2(lib):
+    return _bruteforce(lib, "e5m2") + _bruteforce(lib, "e5m2", Hkv=1, group=6, q_len=8, layout="interleaved",
+                                                  base_pad=8)
 
 
 def pin_bruteforce_bf16(lib):
@@ -251,6 +286,7 @@ def pin_causal_window(lib):
     return fails
 
 
-ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
-            pin_bruteforce_fp8, pin_bruteforce_bf16, pin_uniform_mean, pin_single_key, pin_permutation,
+ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_e5m2_vs_torch, pin_e5m2_closed_form,
+            pin_e5m2_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
+            pin_bruteforce_fp8, pin_bruteforce_e5m2, pin_bruteforce_bf16, pin_uniform_mean, pin_single_key, pin_permutation,
             pin_zero_length, pin_two_key, pin_causal_window]

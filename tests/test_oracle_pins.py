@@ -28,6 +28,8 @@ MUTATIONS = {
     8: "E4M3 subnormals decoded as normals",
     9: "FP16 exponent bias 16",
     10: "lse without the max term",
+    11: "E5M2 exponent bias 16",
+    12: "E5M2 subnormals decoded as normals",
 }
 
 

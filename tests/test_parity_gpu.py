@@ -3,7 +3,7 @@
 Small cases are compared row by row in full (several 128-key tiles, ragged
 tails, every q_len, GQA up to 8, several KV heads, 8-byte-only aligned
 interleaved K/V, zero-length and padded slots, contexts shorter than the verify
-window); the five workload configurations are run at full size in the same
+window); the workload configurations are run at full size in the same
 launch configuration the benchmark uses and compared on all rows where the
 oracle is affordable, otherwise on sampled rows."""
 from __future__ import annotations
@@ -29,7 +29,7 @@ def _lib():
 
 def _small(kind, lens, *, Hkv=1, group=6, q_len=8, page_size=16, layout="separate", base_pad=0, seed=1,
            max_ctx=None, padded=()):
-    D_ = 256 if kind == "fp8" else 128
+    D_ = 128 if kind == "bf16" else 256
     spec = wl.Spec(f"small_{kind}", kind, len(lens), Hkv, Hkv * group, D_, q_len, page_size,
                    max_ctx or max(max(lens), 1), ctx_lens=tuple(lens), padded_slots=tuple(padded), layout=layout,
                    base_pad=base_pad)
@@ -54,6 +54,11 @@ SMALL = [
     ("fp8_page128_tma", "fp8", [2000, 129], dict(page_size=128)),
     ("fp8_interleaved_16B_tma", "fp8", [900, 257], dict(Hkv=2, page_size=64, layout="interleaved")),
     ("fp8_padded_nan", "fp8", [900, 0, 33, 0], dict(padded=(3,))),
+    # E5M2 K/V: the TMA and the cp.async (8-byte aligned) loaders, several tile widths
+    ("e5m2_tiles_tail", "e5m2", [300, 37], {}),
+    ("e5m2_hkv2_interleaved_8B", "e5m2", [700, 129, 0], dict(Hkv=2, page_size=32, layout="interleaved", base_pad=8)),
+    ("e5m2_q1", "e5m2", [1000, 5], dict(q_len=1)),
+    ("e5m2_g8_page80_tma", "e5m2", [1000, 333], dict(group=8, page_size=80)),
     ("bf16_d128", "bf16", [1500, 2048, 17], dict(Hkv=8, group=4, q_len=1)),
     ("bf16_d128_q4_8B", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="interleaved", base_pad=8)),
 ]
@@ -95,6 +100,35 @@ def test_config_b4_l32k():
     check_full(w, dec.out)
 
 
+def test_config_b1_l3297_e5m2():
+    w = _full("b1_l3297_e5m2")
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+
+
+def test_e5m2_every_finite_code():
+    """K and V bytes drawn uniformly from all 248 finite E5M2 codes (subnormals,
+    both zeros, 2^-16 .. 57344), so the decode is exercised on every code."""
+    w = _small("e5m2", [700, 260], page_size=32, seed=13)
+    g = torch.Generator().manual_seed(14)
+    kv = w.kv.cpu()
+    n = w.v_offset - w.k_offset
+    codes = torch.randint(0, 256, (2 * n,), generator=g, dtype=torch.int64)
+    finite = ((codes >> 2) & 31) != 31
+    codes = torch.where(finite, codes, codes & 0x83)      # exponent 31 -> 0 (a subnormal)
+    kv[w.k_offset:w.k_offset + 2 * n] = codes.to(torch.uint8)
+    assert set(kv[w.k_offset:w.k_offset + 2 * n].unique().tolist()) == {c for c in range(256) if (c >> 2) & 31 != 31}
+    w = wl.Workload(**{**w.__dict__, "kv": kv.cuda(), "k_scale": 2.0 / 57344, "v_scale": 1.0 / 57344})
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+
+
 def _sample_rows(w, per_request: int, seed: int) -> np.ndarray:
     s = w.spec
     rng = np.random.default_rng(seed)
@@ -116,6 +150,16 @@ def test_config_b8_l128k_sampled():
     torch.cuda.synchronize()
     assert dec.status() == 0
     check_rows(w, dec.out, _sample_rows(w, 2, 5))
+    assert torch.isfinite(dec.out.float()).all()
+
+
+def test_config_b8_l128k_e5m2_sampled():
+    w = _full("b8_l128k_e5m2")
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_rows(w, dec.out, _sample_rows(w, 2, 6))
     assert torch.isfinite(dec.out.float()).all()
 
 
@@ -163,7 +207,7 @@ def _single(w, b):
                        v_scale=w.v_scale)
 
 
-@pytest.mark.parametrize("name", ["b4_l32k", "b16_mixed", "d128_b8"])
+@pytest.mark.parametrize("name", ["b4_l32k", "b16_mixed", "d128_b8", "b8_l128k_e5m2"])
 def test_batched_equals_single_bitwise(name):
     w = _full(name)
     batched = D.Decoder(w).run().clone()
