@@ -113,6 +113,24 @@ bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D element view of Q [B][q_len][Hq][D] (16-bit elements): (d, query head,
+// verify query, request), boxes of 64 elements x G heads x q_len queries,
+// 128-byte swizzle.  One box is one 64-column atom of an item's packed Q tile,
+// rows in (verify query, head) order.
+bool encode_q_map(CUtensorMap* m, const void* q, const pa_params* p, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p->num_q_heads, (cuuint64_t)p->q_len, (cuuint64_t)p->batch};
+  const cuuint64_t row = (cuuint64_t)D * 2;
+  cuuint64_t strides[3] = {row, row * p->num_q_heads, row * p->num_q_heads * p->q_len};
+  cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)p->q_len, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- kernel timing ----------------------------------------------------------
 struct Timing {
   std::mutex mu;
@@ -204,6 +222,8 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
     a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots) &&
                 encode_kv_map(&a.v_maps[m], v_pages, p, true, slots);
   }
+  // the packed Q tile by TMA (Q is 16-byte aligned); a per-lane copy otherwise
+  a.q_tma = encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
   const long long stall = g_stall_next.exchange(0);
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;

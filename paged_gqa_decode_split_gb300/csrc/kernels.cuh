@@ -18,6 +18,11 @@ struct SplitArgs {
   // use_tma != 0 (16-byte aligned bases and strides)
   CUtensorMap k_maps[4];
   CUtensorMap v_maps[4];
+  // 4-D element view of Q (d, query head, verify query, request) with boxes of
+  // 64 elements x G heads x q_len queries (one 128-byte swizzled atom of the
+  // packed tile); used when q_tma != 0
+  CUtensorMap q_map;
+  int q_tma;
   int use_tma;
   const void* q;               // FP16 (E4M3 / E5M2 paths) or BF16 (BF16 path) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs

@@ -408,7 +408,9 @@ done:
 // Q tile and QK issuer (one warp): per item the warp loads the packed Q tile
 // (row r = qi * G + hl holds query head g*G + hl of verify query qi; K-major,
 // element (r, d) at (d/64)*(NM*128) + r*128 + ((((d%64)/8) ^ (r%8)) * 16) +
-// (d%8)*2) once every QK of the previous item completed (q_empty); lane 0 then
+// (d%8)*2) once every QK of the previous item completed (q_empty): one TMA box
+// per 64-column atom (the 128-byte swizzle of the copy is this layout), or
+// 16-byte copies by every lane when no tensor map could be made; lane 0 then
 // issues QK(j) for the item's tiles (S^T[128 keys x N] = K' Q^T, 16 steps of
 // K = 16, FP32 in TMEM), each once K'(j) is written and S[j&1] is free (the
 // softmax signalled P^T(j-2) after its last read of it), and commits to
@@ -430,16 +432,27 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
     if (!mbar_wait(&M.q_empty, (n & 1) ^ 1, abort)) break;
-    for (int u = lane; u < a.R * kPieces; u += 32) {
-      const int r = u / kPieces, c = u % kPieces;
-      const int qi = r / a.G, hl = r % a.G;
-      const uint16_t* src = q + ((size_t)(x.b * a.q_len + qi) * a.Hq + x.g * a.G + hl) * Fmt::D + c * 8;
-      const uint32_t dst = smem_u32(qbuf + (c >> 3) * (NM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-      cp_async_16(dst, src, 16u);
+    if (a.q_tma) {
+      // one box per 64-column atom: rows (qi, hl) land at r = qi * G + hl
+      if (lane == 0 && !a.withhold_q) {  // withheld only by the timeout test hook
+#pragma unroll
+        for (int c = 0; c < Fmt::D / 64; ++c)
+          tma_load_4d(smem_u32(qbuf + c * L::kQAtom), &a.q_map, 64 * c, x.g * a.G, 0, x.b, &M.q_full);
+        mbar_arrive_expect_tx(&M.q_full, (uint32_t)((Fmt::D / 64) * a.R * 128));
+      }
+    } else {
+      for (int u = lane; u < a.R * kPieces; u += 32) {
+        const int r = u / kPieces, c = u % kPieces;
+        const int qi = r / a.G, hl = r % a.G;
+        const uint16_t* src = q + ((size_t)(x.b * a.q_len + qi) * a.Hq + x.g * a.G + hl) * Fmt::D + c * 8;
+        const uint32_t dst = smem_u32(qbuf + (c >> 3) * (NM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+        cp_async_16(dst, src, 16u);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && !a.withhold_q) mbar_arrive(&M.q_full);
     }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    __syncwarp();
     // the next item's Q rows into L2, so that its Q tile is not a round trip
     // to HBM at the item boundary (each row is D * 2 bytes of one query head)
     if (it + (int)gridDim.x < M.sched.total) {
@@ -451,7 +464,6 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
       }
     }
     if (lane == 0) {
-      if (!a.withhold_q) mbar_arrive(&M.q_full);  // withheld only by the timeout test hook
       ok = mbar_wait(&M.q_full, n & 1, abort);
       for (int jl = 0; ok && jl < nt; ++jl, ++j) {
         if (j >= 2) ok = mbar_wait(&M.p_full[(j - 2) % kPBufs], ((j - 2) / kPBufs) & 1, abort);
@@ -817,19 +829,39 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
     }
     bad |= !mbar_wait(&M.pv_done[(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1, abort);
     tc_fence_after();
+    if constexpr (kHalves * RG <= 48) {
+      // the group's O^T columns into registers, O^T released to the next
+      // item's PV products, then the stores
+      uint32_t r[kHalves][RG];
 #pragma unroll
-    for (int h = 0; h < kHalves; ++h) {
-      uint32_t r[RG];
-      tmem_load_rows(lane_base + kColO + 64 * h + row0, r);
+      for (int h = 0; h < kHalves; ++h) tmem_load_rows(lane_base + kColO + 64 * h + row0, r[h]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.o_free);
 #pragma unroll
-      for (int k = 0; k < RG; ++k) {
-        const int row = row0 + k;
-        if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[k]);
+      for (int h = 0; h < kHalves; ++h) {
+#pragma unroll
+        for (int k = 0; k < RG; ++k) {
+          const int row = row0 + k;
+          if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[h][k]);
+        }
       }
+    } else {
+      // 64 packed rows of D 256: one half at a time (register budget)
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        uint32_t r[RG];
+        tmem_load_rows(lane_base + kColO + 64 * h + row0, r);
+#pragma unroll
+        for (int k = 0; k < RG; ++k) {
+          const int row = row0 + k;
+          if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[k]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.o_free);
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&M.o_free);
     named_bar_sync(bar_id, 128);  // every warp of the group is done with mref and red
     if (gt < RG) M.mref[row0 + gt] = kNoMax;
     named_bar_sync(bar_id, 128);
