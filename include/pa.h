@@ -228,6 +228,59 @@ int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, 
                         const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- workspace bank ---------------------------------------------------------
+ *
+ * A host object that hands out decode workspaces ("panels") so that CUDA
+ * graphs can be captured for several batch sizes without one workspace per
+ * graph ("DFlash2 concurrent long-context attention", section "Why the
+ * single-request optimization was missing from concurrent decode":
+ * workspaces are shared across compatible batch sizes on the same device,
+ * stream and context contract; descending capture allocates the largest
+ * panel once; when a call grows the bank, older panels stay alive because
+ * earlier graphs can still reference them; different streams never share a
+ * panel; section "Operator validation": growing the bank preserves every
+ * pointer handed out before).
+ *
+ * Key of a panel: (device, stream, head_dim, num_kv_heads, num_q_heads,
+ * q_len, max_ctx_len).  pa_bank_workspace returns the key's current panel
+ * when it is large enough for *p (any batch up to the one it was made for),
+ * otherwise it obtains a panel of exactly the needed size from the caller's
+ * allocator, makes it the key's current panel and keeps the older ones.  No
+ * panel is released before pa_bank_destroy.  The bank itself allocates no
+ * device memory, makes no CUDA call and is safe to use from several host
+ * threads; `device` and `stream` are only compared, never used.
+ *
+ * pa_bank_alloc_fn  returns `bytes` bytes of ZERO-FILLED device memory on
+ *                   `device`, 256-byte aligned (the workspace's status word
+ *                   must start at zero), or NULL.  Called with the bank's
+ *                   lock held: it must not call back into the bank.
+ * pa_bank_free_fn   returns a panel to the caller (NULL: the caller keeps
+ *                   ownership of every panel). */
+typedef struct pa_bank pa_bank;
+typedef void* (*pa_bank_alloc_fn)(size_t bytes, int32_t device, void* user);
+typedef void (*pa_bank_free_fn)(void* ptr, size_t bytes, int32_t device, void* user);
+
+/* New empty bank (host), or NULL when alloc is NULL or host memory runs out. */
+pa_bank* pa_bank_create(pa_bank_alloc_fn alloc, pa_bank_free_fn release, void* user);
+
+/* Workspace for a decode call with geometry *p (head_dim 256: pa_decode_fp8 /
+ * pa_decode_e5m2; 128: pa_decode_bf16_d128) on `device` and `stream`:
+ * *workspace and *workspace_bytes (host outputs) are the panel to pass to the
+ * decode call.  Returns PA_OK; PA_ERR_NULL; PA_ERR_SHAPE (device < 0 or a
+ * geometry the decode calls reject); PA_ERR_UNSUPPORTED (head_dim);
+ * PA_ERR_WORKSPACE (the allocator returned NULL); PA_ERR_ALIGN (the allocator
+ * returned memory that is not 256-byte aligned; it is handed back through
+ * pa_bank_free_fn). */
+int pa_bank_workspace(pa_bank* bank, const pa_params* p, int32_t device, void* stream, void** workspace,
+                      size_t* workspace_bytes);
+
+/* Number of panels the bank holds and their total bytes (host outputs). */
+int pa_bank_stats(pa_bank* bank, int64_t* panels, int64_t* bytes);
+
+/* Releases every panel through pa_bank_free_fn and frees the bank.  No decode
+ * call or graph that uses one of its panels may run afterwards. */
+int pa_bank_destroy(pa_bank* bank);
+
 /* ---- status word ------------------------------------------------------------
  * pa_read_status synchronises `stream`, then copies the status word of
  * `workspace` to *flags (host).  pa_clear_status enqueues a reset of it. */

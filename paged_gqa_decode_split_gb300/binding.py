@@ -44,6 +44,10 @@ class pa_params(ctypes.Structure):
 _LIB = None
 _P = ctypes.POINTER
 
+# pa_bank_alloc_fn / pa_bank_free_fn
+BANK_ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p)
+BANK_FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p)
+
 
 def lib_path() -> str:
     return _build.LIB
@@ -70,6 +74,10 @@ def load() -> ctypes.CDLL:
             "pa_decode_e5m2": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_bf16_d128_workspace_bytes": ([pp], sz),
             "pa_decode_bf16_d128": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "pa_bank_create": ([BANK_ALLOC_FN, BANK_FREE_FN, vp], vp),
+            "pa_bank_destroy": ([vp], ctypes.c_int),
+            "pa_bank_workspace": ([vp, pp, i32, vp, _P(vp), _P(sz)], ctypes.c_int),
+            "pa_bank_stats": ([vp, _P(i64), _P(i64)], ctypes.c_int),
             "pa_read_status": ([vp, _P(ctypes.c_uint32), vp], ctypes.c_int),
             "pa_clear_status": ([vp, vp], ctypes.c_int),
             "pa_debug_worklist": ([pp, vp, vp, i32, vp, vp], ctypes.c_int),
@@ -178,6 +186,37 @@ def pa_decode_bf16_d128(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens
     return load().pa_decode_bf16_d128(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                       _ptr(ctx_lens), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
                                       _stream(stream))
+
+
+def pa_bank_create(alloc_fn, free_fn=None):
+    """alloc_fn(nbytes, device) -> device address (int, zero-filled, 256-byte
+    aligned) or 0; free_fn(ptr, nbytes, device) or None.  Returns (handle,
+    keepalive): keep `keepalive` referenced for as long as the bank lives."""
+    a = BANK_ALLOC_FN(lambda n, dev, user: alloc_fn(int(n), int(dev)) or None)
+    f = BANK_FREE_FN(lambda ptr, n, dev, user: free_fn(int(ptr or 0), int(n), int(dev))) if free_fn else \
+        ctypes.cast(None, BANK_FREE_FN)
+    h = load().pa_bank_create(a, f, None)
+    return h, (a, f)
+
+
+def pa_bank_destroy(bank) -> int:
+    return load().pa_bank_destroy(bank)
+
+
+def pa_bank_workspace(bank, p: pa_params, device: int, stream) -> tuple[int, int, int]:
+    """Returns (status, workspace address, workspace bytes).  `stream` is only
+    a key: an int (cudaStream_t), a torch stream or None (the legacy default
+    stream, 0)."""
+    ws, n = ctypes.c_void_p(), ctypes.c_size_t()
+    key = 0 if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    st = load().pa_bank_workspace(bank, ctypes.byref(p), int(device), key, ctypes.byref(ws), ctypes.byref(n))
+    return st, int(ws.value or 0), int(n.value)
+
+
+def pa_bank_stats(bank) -> tuple[int, int, int]:
+    panels, nbytes = ctypes.c_int64(), ctypes.c_int64()
+    st = load().pa_bank_stats(bank, ctypes.byref(panels), ctypes.byref(nbytes))
+    return st, panels.value, nbytes.value
 
 
 def pa_read_status(workspace, stream=None) -> tuple[int, int]:

@@ -222,8 +222,9 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
     a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots) &&
                 encode_kv_map(&a.v_maps[m], v_pages, p, true, slots);
   }
-  // the packed Q tile by TMA (Q is 16-byte aligned); a per-lane copy otherwise
-  a.q_tma = encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
+  // the packed Q tile by TMA together with K and V; with 8-byte aligned K/V
+  // the kernel runs its per-lane copy paths for all three
+  a.q_tma = a.use_tma && encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
   const long long stall = g_stall_next.exchange(0);
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;

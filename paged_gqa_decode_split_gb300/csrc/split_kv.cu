@@ -409,8 +409,8 @@ done:
 // (row r = qi * G + hl holds query head g*G + hl of verify query qi; K-major,
 // element (r, d) at (d/64)*(NM*128) + r*128 + ((((d%64)/8) ^ (r%8)) * 16) +
 // (d%8)*2) once every QK of the previous item completed (q_empty): one TMA box
-// per 64-column atom (the 128-byte swizzle of the copy is this layout), or
-// 16-byte copies by every lane when no tensor map could be made; lane 0 then
+// per 64-column atom (the 128-byte swizzle of the copy is this layout) when
+// K and V are loaded by TMA as well, else 16-byte copies by every lane; lane 0 then
 // issues QK(j) for the item's tiles (S^T[128 keys x N] = K' Q^T, 16 steps of
 // K = 16, FP32 in TMEM), each once K'(j) is written and S[j&1] is free (the
 // softmax signalled P^T(j-2) after its last read of it), and commits to

@@ -18,12 +18,56 @@ def params_for(w: Workload) -> B.pa_params:
                          max_ctx_len=s.max_ctx_len, k_strides=w.k_strides, v_strides=w.v_strides)
 
 
+class WorkspaceBank:
+    """pa_bank over torch device memory: every panel is a zero-filled uint8
+    tensor held here until close() (or until the bank is garbage collected).
+    Grow the bank outside CUDA-graph capture (an eager call first), so that no
+    panel comes from a capture's private memory pool."""
+
+    def __init__(self):
+        self._held: dict[int, torch.Tensor] = {}
+
+        def alloc(nbytes: int, device: int) -> int:
+            t = torch.zeros(nbytes + 256, dtype=torch.uint8, device=torch.device("cuda", device))
+            ptr = (t.data_ptr() + 255) & ~255
+            self._held[ptr] = t
+            return ptr
+
+        def free(ptr: int, nbytes: int, device: int) -> None:
+            self._held.pop(ptr, None)
+
+        self.handle, self._keepalive = B.pa_bank_create(alloc, free)
+        if not self.handle:
+            raise RuntimeError("pa_bank_create failed")
+
+    def workspace(self, p: B.pa_params, device: int, stream=None) -> tuple[int, int]:
+        st, ptr, nbytes = B.pa_bank_workspace(self.handle, p, device, stream)
+        B.check(st, "pa_bank_workspace")
+        return ptr, nbytes
+
+    def stats(self) -> tuple[int, int]:
+        st, panels, nbytes = B.pa_bank_stats(self.handle)
+        B.check(st, "pa_bank_stats")
+        return panels, nbytes
+
+    def close(self) -> None:
+        if self.handle:
+            B.check(B.pa_bank_destroy(self.handle), "pa_bank_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Decoder:
     """Holds the device-side buffers one workload needs (output, workspace,
     scales) and enqueues pa_decode_fp8 / pa_decode_e5m2 / pa_decode_bf16_d128 on
     a stream."""
 
-    def __init__(self, w: Workload, *, with_lse: bool = False):
+    def __init__(self, w: Workload, *, with_lse: bool = False, bank: "WorkspaceBank | None" = None, stream=None):
         if not w.q.is_cuda:
             raise ValueError("the workload must be on a CUDA device")
         self.w = w
@@ -36,8 +80,14 @@ class Decoder:
                   B.pa_decode_bf16_d128_workspace_bytes(self.p))
         if nbytes == 0:
             raise ValueError("libpa rejects this geometry")
-        self.ws_bytes = nbytes
-        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        if bank is not None:
+            # a panel shared with every other decoder of this (device, stream,
+            # contract); such decoders must be called on `stream` only
+            index = dev.index if dev.index is not None else torch.cuda.current_device()
+            self.workspace, self.ws_bytes = bank.workspace(self.p, index, stream)
+        else:
+            self.ws_bytes = nbytes
+            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.out = torch.empty_like(w.q)
         self.lse = (torch.empty(w.q.shape[:3], dtype=torch.float32, device=dev) if (with_lse and not self.fp8)
                     else None)
