@@ -92,13 +92,17 @@ def test_graphs_across_batch_sizes_share_and_grow_the_bank():
     # a later small batch on the grown stream gets the largest panel
     assert D.Decoder(_prefix(w, 2), bank=bank, stream=s_grow).workspace == runs[-1][1].workspace
 
-    # change every captured input in place (Q, lengths with a zero row), replay
-    # the older graphs after the bank grew, and compare bit for bit
+    # change every captured input in place (Q; lengths, with a zero row, kept
+    # within the pages each request's block-table row holds), replay the older
+    # graphs after the bank grew, and compare bit for bit
     gen = torch.Generator(device="cuda").manual_seed(5)
     for k, (wb, dec, g, st) in enumerate(runs):
         wb.q.copy_(torch.randn(wb.q.shape, generator=gen, device="cuda").half())
-        new = torch.randint(0, 6001, (wb.spec.batch,), generator=gen, device="cuda", dtype=torch.int32)
-        new[0] = 0 if k % 2 else new[0]
+        old = wb.ctx_lens.clone()
+        frac = torch.rand(wb.spec.batch, generator=gen, device="cuda")
+        new = torch.minimum((frac * (old.float() + 1)).floor().to(torch.int32), old)
+        if k % 2:
+            new[0] = 0
         wb.ctx_lens.copy_(new)
     torch.cuda.synchronize()
     for wb, dec, g, st in runs:
