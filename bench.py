@@ -198,9 +198,13 @@ def describe(spec) -> str:
 
 
 KIND_TEXT = {"fp8": "FP16 Q, E4M3 K/V per-tensor scales", "e5m2": "FP16 Q, E5M2 K/V per-tensor scales",
-             "bf16": "BF16 Q/K/V"}
-DTYPE_TEXT = {"fp8": "f16xe4m3->f32", "e5m2": "f16xe5m2->f32", "bf16": "bf16->f32"}
-ENTRY_POINT = {"fp8": "pa_decode_fp8", "e5m2": "pa_decode_e5m2", "bf16": "pa_decode_bf16_d128"}
+             "f16": "FP16 Q/K/V", "bf16": "BF16 Q/K/V"}
+DTYPE_TEXT = {"fp8": "f16xe4m3->f32", "e5m2": "f16xe5m2->f32", "f16": "f16->f32", "bf16": "bf16->f32"}
+
+
+def entry_point(spec) -> str:
+    return {"fp8": "pa_decode_fp8", "e5m2": "pa_decode_e5m2", "f16": "pa_decode_f16",
+            "bf16": f"pa_decode_bf16_d{spec.head_dim}"}[spec.kind]
 
 
 def reduce_max(values, dist):
@@ -385,7 +389,7 @@ def run_gpu(args, dist, rank, world, local):
                    "unique_kv_bytes_per_call": unique},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": f"split-KV kernel ({ENTRY_POINT[spec.kind]} main kernel)",
+                     "kernel": f"split-KV kernel ({entry_point(spec)} main kernel)",
                      "kernel_avg_us": split_avg_s * 1e6, "combine_avg_us": comb_ms / max(comb_n, 1) * 1e3,
                      "timed_launches": split_n},
         "gpu_launches": 2 * args.steps,

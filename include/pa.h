@@ -94,7 +94,7 @@ typedef struct pa_caps {
   int32_t page_multiple; /* page_size must be a positive multiple of this */
   int32_t max_ctx;       /* largest max_ctx_len */
   int32_t accum_bits;    /* width of the QK and PV accumulators: 32 */
-  int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8 and pa_decode_e5m2: 256 */
+  int32_t fp8_head_dim;  /* head_dim of pa_decode_fp8, pa_decode_e5m2, pa_decode_f16, pa_decode_bf16_d256: 256 */
   int32_t bf16_head_dim; /* head_dim of pa_decode_bf16_d128: 128 */
   int32_t max_splits;    /* most splits one request is cut into (pa_split_plan's *num_splits) */
   int32_t reserved[6];
@@ -105,7 +105,7 @@ typedef struct pa_params {
   int32_t batch;             /* request slots B, 1 .. max_batch (padded slots have ctx_lens 0) */
   int32_t num_kv_heads;      /* Hkv >= 1 */
   int32_t num_q_heads;       /* Hq = G * Hkv, 1 <= G <= max_group */
-  int32_t head_dim;          /* D: 256 for pa_decode_fp8 / pa_decode_e5m2, 128 for pa_decode_bf16_d128 */
+  int32_t head_dim;          /* D: 128 for pa_decode_bf16_d128, 256 for every other decode call */
   int32_t q_len;             /* verify queries per request, 1 .. max_q_len (bf16: 1 .. max_q_len too) */
   int32_t page_size;         /* tokens per page, a positive multiple of page_multiple */
   int32_t max_pages_per_req; /* block_table row length; >= ceil(max_ctx_len / page_size) */
@@ -211,6 +211,32 @@ int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages
 int pa_decode_e5m2(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale,
                    const float* v_scale, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- 16-bit K/V, head_dim 256 ----------------------------------------------
+ *
+ * The same decode over caches that keep K and V in 16 bits: FP16 Q/K/V
+ * (pa_decode_f16; FP16 KV is one of the cache types that keeps its own graph
+ * set, "DFlash2 concurrent long-context attention", section "Why the
+ * single-request optimization was missing from concurrent decode", and whose
+ * graphs "SM70 attention and quantized projection coverage across TP sizes",
+ * section "Additional findings", checks against FP64) and BF16 Q/K/V
+ * (pa_decode_bf16_d256, the head-dim-256 counterpart of pa_decode_bf16_d128,
+ * "perf(fa2): port decode GQA group-swap into d128 varlen launcher", vllm.cpp
+ * pull request #48).  Arguments, layouts, alignment, workspace
+ * (pa_decode_fp8_workspace_bytes: the workspace depends on head_dim, not on
+ * the element type), errors and results are those of pa_decode_fp8 with
+ * these differences: K and V elements are 2 bytes (512 bytes per key row),
+ * there are no scales, the softmax scale is 1/16, and out is FP16
+ * (pa_decode_f16) or BF16 (pa_decode_bf16_d256).  For BF16 the V values are
+ * rounded to FP16 for the PV product, as in pa_decode_bf16_d128.
+ * lse         (pa_decode_bf16_d256) optional, as in pa_decode_bf16_d128. */
+int pa_decode_f16(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* ctx_lens, void* out, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+int pa_decode_bf16_d256(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- BF16 Q/K/V, head_dim 128 ----------------------------------------------
  *

@@ -73,6 +73,8 @@ def _setup(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_paged_attn_e5m2.argtypes = common + [f32, f32, vp, i32, vp, vp, i32]
     lib.oracle_paged_attn_e5m2.restype = i32
     lib.oracle_paged_attn_bf16.argtypes = common + [vp, i32, vp, vp, i32]
+    lib.oracle_paged_attn_f16.argtypes = common + [vp, i32, vp, vp, i32]
+    lib.oracle_paged_attn_f16.restype = i32
     lib.oracle_paged_attn_bf16.restype = i32
     lib.oracle_max_threads.restype = i32
     lib.oracle_mutation.restype = i32
@@ -126,7 +128,7 @@ def paged_attn(kind: str, *, q: np.ndarray, kv: np.ndarray, k_offset: int, v_off
     """Evaluate the definition for every (or the selected) output rows.
 
     kind          "fp8" (FP16 Q, E4M3 K/V + FP32 scales), "e5m2" (FP16 Q, E5M2
-                  K/V + FP32 scales) or "bf16" (BF16 Q/K/V).
+                  K/V + FP32 scales), "f16" (FP16 Q/K/V) or "bf16" (BF16 Q/K/V).
     q             uint16 bit patterns [B, q_len, Hq, D].
     kv            one uint8 host buffer holding both K and V pages; K element
                   (page, slot, head, d) is at byte k_offset + page*k_strides[0]
@@ -158,8 +160,9 @@ def paged_attn(kind: str, *, q: np.ndarray, kv: np.ndarray, k_offset: int, v_off
     if kind in ("fp8", "e5m2"):
         fn = lib.oracle_paged_attn_fp8 if kind == "fp8" else lib.oracle_paged_attn_e5m2
         rc = fn(*args, float(k_scale), float(v_scale), rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
-    elif kind == "bf16":
-        rc = lib.oracle_paged_attn_bf16(*args, rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
+    elif kind in ("bf16", "f16"):
+        fn = lib.oracle_paged_attn_bf16 if kind == "bf16" else lib.oracle_paged_attn_f16
+        rc = fn(*args, rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
     else:
         raise ValueError(kind)
     if rc != 0:

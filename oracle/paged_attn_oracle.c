@@ -24,7 +24,8 @@
  *            scale per tensor (same section: E4M3 KV, FP16 queries, D = 256 is
  *            the kernel's numerical and shape contract).  An E5M2 cache (a KV
  *            type the same section names beside E4M3) is read the same way
- *            with the E5M2 decoder.
+ *            with the E5M2 decoder, and FP16 or BF16 caches (16-bit K/V, no
+ *            scales) with the binary16 / bfloat16 decoders.
  *   s_j    = (q . k_j) / sqrt(D)
  *   out    = sum_j exp(s_j - max s) v_j / sum_j exp(s_j - max s)
  *   lse    = max s + log(sum_j exp(s_j - max s))
@@ -150,7 +151,7 @@ double oracle_bf16_value(uint16_t bits) {
 
 /* ---- one output row ------------------------------------------------------- */
 
-enum { KV_BF16 = 0, KV_E4M3 = 1, KV_E5M2 = 2 };
+enum { KV_BF16 = 0, KV_E4M3 = 1, KV_E5M2 = 2, KV_F16 = 3 };
 
 typedef struct {
   int B, q_len, Hq, Hkv, D, page_size, max_pages_per_req;
@@ -162,7 +163,7 @@ typedef struct {
   const int32_t* block_table; /* [B][max_pages_per_req] */
   const int32_t* ctx_lens;    /* [B] */
   double k_scale, v_scale;    /* 1.0 for BF16 K/V */
-  int kv_format;              /* KV_BF16, KV_E4M3 or KV_E5M2 */
+  int kv_format;              /* KV_BF16, KV_E4M3, KV_E5M2 or KV_F16 */
   int q_is_bf16;              /* 0: FP16 Q, 1: BF16 Q */
 } problem_t;
 
@@ -175,7 +176,7 @@ static double load_kv(const problem_t* P, const uint8_t* row, int d, double scal
   if (P->kv_format == KV_E5M2) return oracle_e5m2_value(row[d]) * scale;
   uint16_t bits;
   memcpy(&bits, row + 2 * (size_t)d, 2);
-  return oracle_bf16_value(bits);
+  return P->kv_format == KV_F16 ? oracle_f16_value(bits) : oracle_bf16_value(bits);
 }
 
 static const uint8_t* key_row(const problem_t* P, const uint8_t* base, int64_t ps_, int64_t ts_, int64_t hs_,
@@ -322,6 +323,22 @@ int oracle_paged_attn_e5m2(int B, int q_len, int Hq, int Hkv, int D, int page_si
   problem_t P = {B, q_len, Hq, Hkv, D, page_size, max_pages_per_req, q, k_base, v_base,
                  k_page_stride, k_token_stride, k_head_stride, v_page_stride, v_token_stride, v_head_stride,
                  block_table, ctx_lens, (double)k_scale, (double)v_scale, KV_E5M2, 0};
+  return run(&P, rows, n_rows, out, lse, num_threads);
+}
+
+/*
+ * FP16 Q, K, V (no scales).  Strides are in bytes.  Same row selection and
+ * outputs as oracle_paged_attn_fp8.
+ */
+int oracle_paged_attn_f16(int B, int q_len, int Hq, int Hkv, int D, int page_size, int max_pages_per_req,
+                          const uint16_t* q, const uint8_t* k_base, const uint8_t* v_base,
+                          int64_t k_page_stride, int64_t k_token_stride, int64_t k_head_stride,
+                          int64_t v_page_stride, int64_t v_token_stride, int64_t v_head_stride,
+                          const int32_t* block_table, const int32_t* ctx_lens,
+                          const int32_t* rows, int n_rows, double* out, double* lse, int num_threads) {
+  problem_t P = {B, q_len, Hq, Hkv, D, page_size, max_pages_per_req, q, k_base, v_base,
+                 k_page_stride, k_token_stride, k_head_stride, v_page_stride, v_token_stride, v_head_stride,
+                 block_table, ctx_lens, 1.0, 1.0, KV_F16, 0};
   return run(&P, rows, n_rows, out, lse, num_threads);
 }
 

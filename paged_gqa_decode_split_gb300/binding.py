@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
             "pa_decode_e5m2": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_bf16_d128_workspace_bytes": ([pp], sz),
             "pa_decode_bf16_d128": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "pa_decode_bf16_d256": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "pa_decode_f16": ([pp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_bank_create": ([BANK_ALLOC_FN, BANK_FREE_FN, vp], vp),
             "pa_bank_destroy": ([vp], ctypes.c_int),
             "pa_bank_workspace": ([vp, pp, i32, vp, _P(vp), _P(sz)], ctypes.c_int),
@@ -217,6 +219,19 @@ def pa_bank_stats(bank) -> tuple[int, int, int]:
     panels, nbytes = ctypes.c_int64(), ctypes.c_int64()
     st = load().pa_bank_stats(bank, ctypes.byref(panels), ctypes.byref(nbytes))
     return st, panels.value, nbytes.value
+
+
+def pa_decode_f16(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, out, workspace, workspace_bytes: int,
+                  stream=None) -> int:
+    return load().pa_decode_f16(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                _ptr(ctx_lens), _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def pa_decode_bf16_d256(p: pa_params, q, k_pages, v_pages, block_table, ctx_lens, out, lse, workspace,
+                        workspace_bytes: int, stream=None) -> int:
+    return load().pa_decode_bf16_d256(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                      _ptr(ctx_lens), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                      _stream(stream))
 
 
 def pa_read_status(workspace, stream=None) -> tuple[int, int]:

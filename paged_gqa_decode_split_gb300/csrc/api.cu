@@ -92,18 +92,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 4-D byte view of K or V: (row byte 0..255, KV head, slot, page), boxes of
-// 128 bytes x 1 head x `slots` slots, 128-byte swizzle.  A box taller than a
-// page is clipped to the page (the loader never uses a box taller than the
-// piece of a page it copies).
-bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v, unsigned slots) {
+// 4-D byte view of K or V: (row byte 0..row_bytes-1, KV head, slot, page),
+// boxes of 128 bytes x 1 head x `slots` slots, 128-byte swizzle.  A box taller
+// than a page is clipped to the page (the loader never uses a box taller than
+// the piece of a page it copies).
+bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v, unsigned slots, int row_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const long long hs = v ? p->v_head_stride : p->k_head_stride;
   const long long ts = v ? p->v_token_stride : p->k_token_stride;
   const long long ps = v ? p->v_page_stride : p->k_page_stride;
-  cuuint64_t dims[4] = {256, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size, (cuuint64_t)p->num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)(p->num_kv_heads == 1 ? 256 : hs), (cuuint64_t)ts, (cuuint64_t)ps};
+  cuuint64_t dims[4] = {(cuuint64_t)row_bytes, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size,
+                        (cuuint64_t)p->num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)(p->num_kv_heads == 1 ? row_bytes : hs), (cuuint64_t)ts, (cuuint64_t)ps};
   cuuint32_t box[4] = {128, 1, slots < (unsigned)p->page_size ? slots : (cuuint32_t)p->page_size, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   for (cuuint64_t s : strides)
@@ -171,17 +172,19 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
                   const int32_t* block_table, const int32_t* ctx_lens, const float* k_scale, const float* v_scale,
                   void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr,
                   bool clear_status = false) {
-  const bool bf16 = fmt == kKvBf16;
-  const int D = bf16 ? 128 : 256;
+  const bool scaled = fmt == kKvE4m3 || fmt == kKvE5m2;  // 8-bit K/V with FP32 per-tensor scales
+  const bool bf16_out = fmt == kKvBf16 || fmt == kKvBf16D256;
+  const int D = fmt == kKvBf16 ? 128 : 256;
+  const int row_bytes = D * (scaled ? 1 : 2);
   int R = 0;
   int st = check_geometry(p, D, &R);
   if (st != PA_OK) return st;
   if (!q || !k_pages || !v_pages || !block_table || !ctx_lens || !out) return PA_ERR_NULL;
-  if (!bf16 && (!k_scale || !v_scale)) return PA_ERR_NULL;
+  if (scaled && (!k_scale || !v_scale)) return PA_ERR_NULL;
   if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16))) return PA_ERR_ALIGN;
   if (!aligned(k_pages, 8) || !aligned(v_pages, 8) || !aligned(block_table, 4) || !aligned(ctx_lens, 4))
     return PA_ERR_ALIGN;
-  if (!bf16 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return PA_ERR_ALIGN;
+  if (scaled && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return PA_ERR_ALIGN;
   const int s_max = max_splits_for(p->max_ctx_len);
   const WsLayout L = ws_layout(p->batch, p->num_kv_heads, s_max, R, D);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes_given < L.total) return PA_ERR_WORKSPACE;
@@ -219,8 +222,8 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.use_tma = strides16(p, k_pages, v_pages);
   for (int m = 0; m < 4 && a.use_tma; ++m) {
     const unsigned slots = 128u >> m;
-    a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots) &&
-                encode_kv_map(&a.v_maps[m], v_pages, p, true, slots);
+    a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots, row_bytes) &&
+                encode_kv_map(&a.v_maps[m], v_pages, p, true, slots, row_bytes);
   }
   // the packed Q tile by TMA together with K and V; with 8-byte aligned K/V
   // the kernel runs its per-lane copy paths for all three
@@ -242,7 +245,7 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   c.panel_ml = a.panel_ml;
   c.panel_o = a.panel_o;
   c.bad = bad;
-  c.out_scale_ptr = bf16 ? nullptr : v_scale;
+  c.out_scale_ptr = scaled ? v_scale : nullptr;
   c.out_scale_mul = 1.0f;
   c.out = out;
   c.lse = lse;
@@ -250,7 +253,7 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   c.max_ctx = a.max_ctx, c.s_max = s_max;
   timing_slot(1, &e0, &e1);
   if (e0) cudaEventRecord(e0, stream);
-  if (launch_combine(c, bf16, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_combine(c, bf16_out, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (e1) cudaEventRecord(e1, stream);
   return PA_OK;
 }
@@ -351,6 +354,20 @@ int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages
   if (sst != PA_OK) return sst;
   return decode_common(kKvE4m3, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
                        scratch, kNoallocScratchBytes, stream, /*clear_status=*/true);
+}
+
+int pa_decode_f16(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* ctx_lens, void* out, void* workspace,
+                  size_t workspace_bytes_given, void* stream) {
+  return decode_common(kKvF16, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, nullptr,
+                       workspace, workspace_bytes_given, stream);
+}
+
+int pa_decode_bf16_d256(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse, void* workspace,
+                        size_t workspace_bytes_given, void* stream) {
+  return decode_common(kKvBf16D256, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, lse,
+                       workspace, workspace_bytes_given, stream);
 }
 
 int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, const void* v_pages,

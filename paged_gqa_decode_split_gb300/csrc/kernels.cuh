@@ -8,8 +8,9 @@
 namespace pa {
 
 // Element formats of the split kernel: FP16 Q with E4M3 or E5M2 K/V (head_dim
-// 256, FP32 per-tensor scales), or BF16 Q/K/V (head_dim 128).
-enum KvFormat : int { kKvE4m3 = 0, kKvBf16 = 1, kKvE5m2 = 2 };
+// 256, FP32 per-tensor scales), BF16 Q/K/V (head_dim 128 or 256), FP16 Q/K/V
+// (head_dim 256).
+enum KvFormat : int { kKvE4m3 = 0, kKvBf16 = 1, kKvE5m2 = 2, kKvF16 = 3, kKvBf16D256 = 4 };
 
 // Split-KV kernel arguments (every element format).
 struct SplitArgs {
@@ -54,6 +55,12 @@ struct CombineArgs {
 
 int split_smem_bytes();
 cudaError_t launch_split(const SplitArgs& a, KvFormat fmt, int grid, cudaStream_t stream);
+// per-format launchers behind launch_split (split_kv_<format>.cu)
+cudaError_t launch_split_e4m3(const SplitArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_split_e5m2(const SplitArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_split_f16(const SplitArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_split_bf16_d128(const SplitArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_split_bf16_d256(const SplitArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream);
 cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
                                   int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream);

@@ -64,8 +64,9 @@ class WorkspaceBank:
 
 class Decoder:
     """Holds the device-side buffers one workload needs (output, workspace,
-    scales) and enqueues pa_decode_fp8 / pa_decode_e5m2 / pa_decode_bf16_d128 on
-    a stream."""
+    scales) and enqueues the decode call of its kind on a stream:
+    pa_decode_fp8 ("fp8"), pa_decode_e5m2 ("e5m2"), pa_decode_f16 ("f16"),
+    pa_decode_bf16_d128 / pa_decode_bf16_d256 ("bf16", head_dim 128 / 256)."""
 
     def __init__(self, w: Workload, *, with_lse: bool = False, bank: "WorkspaceBank | None" = None, stream=None):
         if not w.q.is_cuda:
@@ -76,8 +77,8 @@ class Decoder:
         dev = w.q.device
         self.kind = s.kind
         self.fp8 = s.kind in ("fp8", "e5m2")   # 8-bit K/V with per-tensor scales
-        nbytes = (B.pa_decode_fp8_workspace_bytes(self.p) if self.fp8 else
-                  B.pa_decode_bf16_d128_workspace_bytes(self.p))
+        nbytes = (B.pa_decode_bf16_d128_workspace_bytes(self.p) if s.head_dim == 128 else
+                  B.pa_decode_fp8_workspace_bytes(self.p))
         if nbytes == 0:
             raise ValueError("libpa rejects this geometry")
         if bank is not None:
@@ -89,7 +90,7 @@ class Decoder:
             self.ws_bytes = nbytes
             self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         self.out = torch.empty_like(w.q)
-        self.lse = (torch.empty(w.q.shape[:3], dtype=torch.float32, device=dev) if (with_lse and not self.fp8)
+        self.lse = (torch.empty(w.q.shape[:3], dtype=torch.float32, device=dev) if (with_lse and s.kind == "bf16")
                     else None)
         self.scales = torch.tensor([w.k_scale, w.v_scale], dtype=torch.float32, device=dev)
 
@@ -108,8 +109,12 @@ class Decoder:
             return fn(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
                       self.scales.data_ptr(), self.scales.data_ptr() + 4, self.out, self.workspace, self.ws_bytes,
                       stream)
-        return B.pa_decode_bf16_d128(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
-                                     self.out, self.lse, self.workspace, self.ws_bytes, stream)
+        if self.kind == "f16":
+            return B.pa_decode_f16(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens,
+                                   self.out, self.workspace, self.ws_bytes, stream)
+        fn = B.pa_decode_bf16_d128 if w.spec.head_dim == 128 else B.pa_decode_bf16_d256
+        return fn(self.p, w.q, kv + w.k_offset, kv + w.v_offset, w.block_table, w.ctx_lens, self.out, self.lse,
+                  self.workspace, self.ws_bytes, stream)
 
     def run(self, stream=None) -> torch.Tensor:
         B.check(self(stream), "decode")

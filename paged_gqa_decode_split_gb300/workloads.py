@@ -22,7 +22,8 @@ float8_e4m3fn conversion.  E5M2 K/V (a cache type that keeps its own graph
 set beside E4M3: "DFlash2 concurrent long-context attention", section "Why the
 single-request optimization was missing from concurrent decode") follows the
 same recipe with the format's largest finite value, 57344, in place of 448 and
-torch's float8_e5m2 conversion.  Pages are assigned to requests through a random
+torch's float8_e5m2 conversion.  FP16 and BF16 K/V (16-bit caches, no
+scales) are the N(0, 1) draws rounded to the element type.  Pages are assigned to requests through a random
 permutation of the pool; block-table entries past a request's last page are -1
 and must never be read.  Padded batch slots have ctx_len 0, Q = NaN and a block
 table row of -1.
@@ -44,7 +45,8 @@ class Spec:
     """Shape and structure of one workload (values are drawn by ``generate``)."""
 
     name: str
-    kind: str                      # "fp8": FP16 Q + E4M3 K/V, "e5m2": FP16 Q + E5M2 K/V, "bf16": BF16 Q/K/V
+    kind: str                      # "fp8": FP16 Q + E4M3 K/V, "e5m2": FP16 Q + E5M2 K/V,
+                                   # "f16": FP16 Q/K/V, "bf16": BF16 Q/K/V
     batch: int
     num_kv_heads: int
     num_q_heads: int
@@ -103,15 +105,17 @@ SPECS: dict[str, Spec] = {
     "b16_mixed": Spec("b16_mixed", "fp8", 16, 2, 12, 256, 8, 3296, 262144, ctx_range=(0, 262144),
                       zero_slots=(4, 9), padded_slots=(13, 14, 15), layout="interleaved", base_pad=8),
 }
-# E5M2 K/V on the E4M3 configurations' shapes
+# E5M2, FP16 and BF16 K/V on the E4M3 configurations' shapes
 for _n in ("b1_l3297", "b8_l128k"):
-    SPECS[_n + "_e5m2"] = dataclasses.replace(SPECS[_n], name=_n + "_e5m2", kind="e5m2")
+    for _k in ("e5m2", "f16", "bf16"):
+        SPECS[f"{_n}_{_k}"] = dataclasses.replace(SPECS[_n], name=f"{_n}_{_k}", kind=_k)
 for _b in (1, 2, 4, 8):
     SPECS[f"d128_b{_b}"] = Spec(f"d128_b{_b}", "bf16", _b, 8, 32, 128, 1, 16, 32768, ctx_range=(1024, 32768))
 
 CONFIG_SEED = {"b1_l3297": 1000, "b4_l32k": 1001, "b8_l128k": 1002, "b16_mixed": 1003,
                "d128_b1": 1004, "d128_b2": 1014, "d128_b4": 1024, "d128_b8": 1034,
-               "b1_l3297_e5m2": 1005, "b8_l128k_e5m2": 1006}
+               "b1_l3297_e5m2": 1005, "b8_l128k_e5m2": 1006, "b1_l3297_f16": 1007, "b8_l128k_f16": 1008,
+               "b1_l3297_bf16": 1009, "b8_l128k_bf16": 1010}
 
 
 def working_set_seed(name: str, w: int) -> int:
@@ -184,9 +188,10 @@ def generate(spec: Spec, seed: int, device: str | torch.device = "cpu",
         vb, v_scale = _quantize(vx, spec.kind)
         del vx
     else:
-        kb = kx.to(torch.bfloat16).view(torch.uint8).reshape(*shape[:3], D * 2)
+        edt = torch.bfloat16 if spec.kind == "bf16" else torch.float16
+        kb = kx.to(edt).view(torch.uint8).reshape(*shape[:3], D * 2)
         del kx
-        vb = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        vb = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(edt)
         vb = vb.view(torch.uint8).reshape(*shape[:3], D * 2)
         k_scale = v_scale = 1.0
     row = D * spec.elem_bytes

@@ -25,8 +25,8 @@ def run_oracle(w: wl.Workload, rows=None, lib=None, num_threads: int = 0):
 
 def _elements(w: wl.Workload, which: str, b: int, g: int, n: int) -> torch.Tensor:
     """Dense float64 K or V rows 0..n-1 of request b, KV head g, decoded with
-    torch's own float8_e4m3fn / float8_e5m2 / bfloat16 casts (not the oracle's
-    decoders)."""
+    torch's own float8_e4m3fn / float8_e5m2 / float16 / bfloat16 casts (not the
+    oracle's decoders)."""
     s = w.spec
     kv = w.kv.detach().cpu()
     off = w.k_offset if which == "k" else w.v_offset
@@ -45,7 +45,7 @@ def _elements(w: wl.Workload, which: str, b: int, g: int, n: int) -> torch.Tenso
         scale = w.k_scale if which == "k" else w.v_scale
         dtype = torch.float8_e4m3fn if s.kind == "fp8" else torch.float8_e5m2
         return raw.view(dtype).to(torch.float64) * torch.tensor(scale, dtype=torch.float32).double()
-    return raw.view(torch.bfloat16).to(torch.float64)
+    return raw.view(torch.bfloat16 if s.kind == "bf16" else torch.float16).to(torch.float64)
 
 
 def dense_reference(w: wl.Workload):

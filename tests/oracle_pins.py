@@ -156,7 +156,12 @@ def pin_bruteforce_e5m2(lib):
 
 
 def pin_bruteforce_bf16(lib):
-    return _bruteforce(lib, "bf16", Hkv=2, group=4, q_len=1)
+    return _bruteforce(lib, "bf16", Hkv=2, group=4, q_len=1) + _bruteforce(lib, "bf16", D=256)
+
+
+def pin_bruteforce_f16(lib):
+    return _bruteforce(lib, "f16") + _bruteforce(lib, "f16", Hkv=1, group=6, q_len=8, layout="interleaved",
+                                                 base_pad=8)
 
 
 def pin_uniform_mean(lib):
@@ -288,5 +293,5 @@ def pin_causal_window(lib):
 
 ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_e5m2_vs_torch, pin_e5m2_closed_form,
             pin_e5m2_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
-            pin_bruteforce_fp8, pin_bruteforce_e5m2, pin_bruteforce_bf16, pin_uniform_mean, pin_single_key, pin_permutation,
+            pin_bruteforce_fp8, pin_bruteforce_e5m2, pin_bruteforce_bf16, pin_bruteforce_f16, pin_uniform_mean, pin_single_key, pin_permutation,
             pin_zero_length, pin_two_key, pin_causal_window]

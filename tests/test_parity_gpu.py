@@ -28,8 +28,8 @@ def _lib():
 
 
 def _small(kind, lens, *, Hkv=1, group=6, q_len=8, page_size=16, layout="separate", base_pad=0, seed=1,
-           max_ctx=None, padded=()):
-    D_ = 128 if kind == "bf16" else 256
+           max_ctx=None, padded=(), D=None):
+    D_ = D or (128 if kind == "bf16" else 256)
     spec = wl.Spec(f"small_{kind}", kind, len(lens), Hkv, Hkv * group, D_, q_len, page_size,
                    max_ctx or max(max(lens), 1), ctx_lens=tuple(lens), padded_slots=tuple(padded), layout=layout,
                    base_pad=base_pad)
@@ -59,6 +59,16 @@ SMALL = [
     ("e5m2_hkv2_interleaved_8B", "e5m2", [700, 129, 0], dict(Hkv=2, page_size=32, layout="interleaved", base_pad=8)),
     ("e5m2_q1", "e5m2", [1000, 5], dict(q_len=1)),
     ("e5m2_g8_page80_tma", "e5m2", [1000, 333], dict(group=8, page_size=80)),
+    # 16-bit K/V at D 256 (512-byte rows, two staging fills per tile): TMA and
+    # cp.async loaders, several tile widths
+    ("f16_tiles_tail", "f16", [300, 37], {}),
+    ("f16_hkv2_interleaved_8B", "f16", [700, 129, 0], dict(Hkv=2, page_size=32, layout="interleaved", base_pad=8)),
+    ("f16_q1_page80_tma", "f16", [1000, 5], dict(q_len=1, page_size=80)),
+    ("f16_g8", "f16", [513, 64], dict(group=8)),
+    ("bf16_d256_tiles_tail", "bf16", [300, 37], dict(D=256)),
+    ("bf16_d256_hkv2_interleaved_8B", "bf16", [700, 129, 0],
+     dict(D=256, Hkv=2, page_size=32, layout="interleaved", base_pad=8)),
+    ("bf16_d256_g4_q1", "bf16", [2000, 17], dict(D=256, Hkv=2, group=4, q_len=1, page_size=64)),
     ("bf16_d128", "bf16", [1500, 2048, 17], dict(Hkv=8, group=4, q_len=1)),
     ("bf16_d128_q4_8B", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="interleaved", base_pad=8)),
 ]
@@ -107,6 +117,16 @@ def test_config_b1_l3297_e5m2():
     torch.cuda.synchronize()
     assert dec.status() == 0
     check_full(w, dec.out)
+
+
+@pytest.mark.parametrize("name", ["b1_l3297_f16", "b1_l3297_bf16"])
+def test_config_b1_l3297_16bit(name):
+    w = _full(name)
+    dec = D.Decoder(w, with_lse=w.spec.kind == "bf16")
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out, dec.lse)
 
 
 def test_e5m2_every_finite_code():
@@ -163,6 +183,17 @@ def test_config_b8_l128k_e5m2_sampled():
     assert torch.isfinite(dec.out.float()).all()
 
 
+@pytest.mark.parametrize("name", ["b8_l128k_f16", "b8_l128k_bf16"])
+def test_config_b8_l128k_16bit_sampled(name):
+    w = _full(name)
+    dec = D.Decoder(w)
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_rows(w, dec.out, _sample_rows(w, 2, 7))
+    assert torch.isfinite(dec.out.float()).all()
+
+
 def test_config_b16_mixed_sampled():
     w = _full("b16_mixed")
     dec = D.Decoder(w)
@@ -207,7 +238,7 @@ def _single(w, b):
                        v_scale=w.v_scale)
 
 
-@pytest.mark.parametrize("name", ["b4_l32k", "b16_mixed", "d128_b8", "b8_l128k_e5m2"])
+@pytest.mark.parametrize("name", ["b4_l32k", "b16_mixed", "d128_b8", "b8_l128k_e5m2", "b8_l128k_f16"])
 def test_batched_equals_single_bitwise(name):
     w = _full(name)
     batched = D.Decoder(w).run().clone()
