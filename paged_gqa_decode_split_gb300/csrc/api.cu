@@ -77,7 +77,7 @@ bool strides16(const pa_params* p, const void* k, const void* v) {
 }
 
 // ---- TMA tensor maps ----------------------------------------------------------
-// The driver's tensor-map encoder, fetched through the runtime so the library
+// The CUDA driver API's tensor-map encoder, fetched through the runtime so the library
 // does not link libcuda directly.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::once_flag once;
