@@ -188,6 +188,32 @@ def test_e5m2_entry_validates(lib):
     assert lib.pa_decode_e5m2(None, *([ctypes.c_void_p(FAKE)] * 9), 1 << 30, None) == B.PA_ERR_NULL
 
 
+def test_16bit_d256_entries_validate(lib):
+    """pa_decode_f16 and pa_decode_bf16_d256 take no scales and run the D 256 checks."""
+    p = _params()
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, out=FAKE, lse=None, ws=FAKE, n=1 << 40)
+
+    def f16(params=p, **o):
+        a = {**ok, **o}
+        return B.pa_decode_f16(params, a["q"], a["k"], a["v"], a["bt"], a["cl"], a["out"], a["ws"], a["n"], 0)
+
+    def bf16(params=p, **o):
+        a = {**ok, **o}
+        return B.pa_decode_bf16_d256(params, a["q"], a["k"], a["v"], a["bt"], a["cl"], a["out"], a["lse"], a["ws"],
+                                     a["n"], 0)
+    for call in (f16, bf16):
+        for arg in ("q", "k", "v", "bt", "cl", "out"):
+            assert call(**{arg: 0}) == B.PA_ERR_NULL, arg
+        assert call(q=FAKE + 8) == B.PA_ERR_ALIGN
+        assert call(k=FAKE + 4) == B.PA_ERR_ALIGN
+        assert call(ws=0) == B.PA_ERR_WORKSPACE
+        assert call(n=B.pa_decode_fp8_workspace_bytes(p) - 1) == B.PA_ERR_WORKSPACE
+        assert call(params=_params(head_dim=128)) == B.PA_ERR_UNSUPPORTED
+        assert call(params=_params(batch=0)) == B.PA_ERR_SHAPE
+    assert bf16(lse=FAKE + 4) == B.PA_ERR_ALIGN
+    assert lib.pa_decode_f16(None, *([ctypes.c_void_p(FAKE)] * 7), 1 << 30, None) == B.PA_ERR_NULL
+
+
 def test_bf16_entry_validates(lib):
     p = _params(head_dim=128, num_kv_heads=8, num_q_heads=32, q_len=1, page_size=16, max_pages_per_req=2048,
                 max_ctx_len=32768, k_strides=(16 * 8 * 256, 8 * 256, 256), v_strides=(16 * 8 * 256, 8 * 256, 256))
