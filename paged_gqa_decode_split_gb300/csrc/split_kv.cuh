@@ -311,6 +311,9 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
   WaitCtl* abort = &M.ctl;
   const int ps = a.page_size;
   const uint32_t dst_base = smem_u32(stage);
+  // K and V are read once per call: evict them from L2 first, so that the
+  // split partials the combine kernel reads next stay resident
+  const uint64_t once = l2_policy_evict_first();
   uint32_t f = 0;  // fills issued
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
     const Item x = sched_item(M.sched, a.B, it);
@@ -353,8 +356,8 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
             for (int m = 0; m < 4; ++m) {
               const int box = kTileKeys >> m;  // 128, 64, 32, 16 slots
               while (left >= box) {
-                tma_load_4d(dst_base + rr * 128, maps + m, 256 * h, x.g, sl, pg, full);
-                tma_load_4d(dst_base + 16384 + rr * 128, maps + m, 256 * h + 128, x.g, sl, pg, full);
+                tma_load_4d_hint(dst_base + rr * 128, maps + m, 256 * h, x.g, sl, pg, full, once);
+                tma_load_4d_hint(dst_base + 16384 + rr * 128, maps + m, 256 * h + 128, x.g, sl, pg, full, once);
                 bytes += box * 256;
                 rr += box, sl += box, left -= box;
               }
