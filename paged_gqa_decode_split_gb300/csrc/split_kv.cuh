@@ -725,6 +725,9 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
   const int bar_id = kSoftmaxBar + grp;
   const float c_log2 = Fmt::score_scale(a.k_scale);
   const uint32_t lane_base = tb + ((uint32_t)(32 * i) << 16);
+  // the split partials are read back by the combine kernel right after this
+  // grid: keep their L2 lines
+  const uint64_t keep = l2_policy_evict_last();
   const int rbase = BF::base(lane);  // rows row0+rbase .. +CNT-1 of every butterfly result
   uint32_t j = 0, nvote = 0;
   bool bad = false;
@@ -902,7 +905,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
 #pragma unroll
         for (int k = 0; k < RG; ++k) {
           const int row = row0 + k;
-          if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[h][k]);
+          if (row < a.R) st_global_hint(a.panel_o + (pi + row) * Fmt::D + h * 128 + gt, __uint_as_float(r[h][k]), keep);
         }
       }
     } else {
@@ -914,7 +917,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
 #pragma unroll
         for (int k = 0; k < RG; ++k) {
           const int row = row0 + k;
-          if (row < a.R) a.panel_o[(pi + row) * Fmt::D + h * 128 + gt] = __uint_as_float(r[k]);
+          if (row < a.R) st_global_hint(a.panel_o + (pi + row) * Fmt::D + h * 128 + gt, __uint_as_float(r[k]), keep);
         }
       }
       tc_fence_before();
