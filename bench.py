@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -64,13 +65,24 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and blank space collapsed,
+    so that an edit to comments alone keeps the hash (the sources hold no
+    comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the code of every csrc/*.cu, *.cuh (comments excluded): the ncu
+    traffic recorded under profiles/ is used only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_split_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -40,7 +40,7 @@ int sm_count(int dev) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Geometry checks shared by both variants.  *R receives G * q_len.
+// Geometry checks shared by every decode call.  *R receives G * q_len.
 int check_geometry(const pa_params* p, int head_dim, int* R) {
   if (p == nullptr) return PA_ERR_NULL;
   if (p->head_dim != head_dim) return PA_ERR_UNSUPPORTED;

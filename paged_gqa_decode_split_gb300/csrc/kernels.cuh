@@ -25,12 +25,12 @@ struct SplitArgs {
   CUtensorMap q_map;
   int q_tma;
   int use_tma;
-  const void* q;               // FP16 (E4M3 / E5M2 paths) or BF16 (BF16 path) [B][q_len][Hq][D]
+  const void* q;               // FP16 or BF16 (the BF16 formats) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs
   const uint8_t* v;
   const int32_t* block_table;  // [B][mpr]
   const int32_t* ctx_lens;     // [B]
-  const float* k_scale;        // E4M3 / E5M2 paths only
+  const float* k_scale;        // 8-bit K/V formats only (E4M3, E5M2)
   float2* panel_ml;            // (m in log2 units, l) per (item, row)
   float* panel_o;              // unnormalised O per (item, row, d); 8-bit paths: without v_scale
   uint32_t* status;
@@ -48,7 +48,7 @@ struct CombineArgs {
   const uint32_t* bad;
   const float* out_scale_ptr;  // nullable: output is multiplied by *out_scale_ptr * out_scale_mul
   float out_scale_mul;
-  void* out;                   // FP16 (8-bit K/V paths) or BF16 (BF16 path)
+  void* out;                   // FP16, or BF16 for the BF16 formats
   float* lse;                  // nullable
   int B, Hkv, Hq, G, q_len, R, D, max_ctx, s_max;
 };
