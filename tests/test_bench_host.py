@@ -76,3 +76,16 @@ def test_warmup_floor():
     r = subprocess.run([sys.executable, "bench.py", "--warmup", "2"], cwd=ROOT, capture_output=True, text=True,
                        timeout=120)
     assert r.returncode != 0
+
+
+def test_code_hash_ignores_comments_only():
+    """The recorded ncu traffic stays valid across comment edits, not code edits."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    a = "int f(int x) {  // doubles x\n  return 2 * x; /* plain */\n}\n"
+    b = "// a new header line\nint f(int x) {\n  /* changed\n comment */ return 2 * x;\n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert len(bench.kernel_source_hash()) == 16
