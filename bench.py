@@ -40,6 +40,7 @@ DEFAULT_WORKLOAD = "b8_l128k"
 METRIC = "µs per decode-attention call and effective KV GB/s (% of HBM peak) @B8/128K"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+NAMEPLATE_HBM_GBS = 8000.0  # GB300 HBM3e nameplate, for context next to the measured peak
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kernel_b8_l128k_traffic.json")
 
 
@@ -392,13 +393,15 @@ def run_gpu(args, dist, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "us_per_call": ms / args.steps * 1e3,
         "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "pct_of_nameplate_8tbs": 100.0 * value / world / NAMEPLATE_HBM_GBS,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_TEXT[spec.kind],
         "data": "synthetic",
         "config": {"workload": describe(spec),
                    "global_batch": spec.batch * world, "seq_len": spec.max_ctx_len,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "working_sets": nsets, "l2": l2_note,
-                   "unique_kv_bytes_per_call": unique},
+                   "unique_kv_bytes_per_call": unique,
+                   "l2_bytes": int(getattr(props, "L2_cache_size", 0) or 0)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": f"split-KV kernel ({entry_point(spec)} main kernel)",
