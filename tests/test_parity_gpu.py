@@ -332,6 +332,34 @@ def test_gather_bit_exact(layout, pad):
                 assert np.array_equal(got[b, g, :L], want)
 
 
+def test_all_zero_batch_writes_zeros():
+    """Every request of the batch has length 0 (an all-padding batch): no work
+    item exists, every output element is +0.0, LSE is -inf and no flag is set;
+    then the same decoder serves live lengths again."""
+    for kind, kw in (("fp8", {}), ("f16", {}), ("bf16", dict(D=256)), ("bf16", dict(Hkv=8, group=4, q_len=1))):
+        w = _small(kind, [0, 0, 0], max_ctx=4000, **kw)
+        w.q.fill_(float("nan"))
+        dec = D.Decoder(w, with_lse=(kind == "bf16"))
+        dec.out.fill_(7.0)
+        dec.run()
+        torch.cuda.synchronize()
+        assert dec.status() == 0
+        assert torch.all(dec.out == 0) and not torch.signbit(dec.out.float()).any(), kind
+        if dec.lse is not None:
+            assert torch.all(dec.lse == float("-inf"))
+    w = _small("fp8", [0, 500, 0], max_ctx=4000, seed=3)
+    dec = D.Decoder(w)
+    w.ctx_lens.zero_()
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0 and torch.all(dec.out == 0)
+    w.ctx_lens.copy_(torch.tensor([0, 500, 0], dtype=torch.int32))
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
+
+
 # ------------------------------------------------------------ input checks --
 
 def test_bad_page_flags_and_zeros_request():
