@@ -28,8 +28,9 @@
 // online softmax of a row is a reduction across lanes (warp shuffles).
 //
 // Warp roles (20 warps; warp w runs on sub-partition w % 4):
-//   3  K loader   one thread: TMA (or the warp: cp.async for 8-byte aligned
-//                 data) of block-table-gathered K rows, a tile at a time
+//   3  K loader   one thread: TMA (or the warp: TMA for pages shorter than a
+//                 tile, cp.async for 8-byte aligned data) of block-table-
+//                 gathered K rows, a tile at a time
 //   9  V loader   the same for V
 //   11 Q + QK     the packed Q tile of each item (128-byte swizzle); one
 //                 thread issues the QK tcgen05.mma products
@@ -372,6 +373,61 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
           atomicOr(a.bad + x.b, 1u);
         }
         mbar_arrive_expect_tx(full, bytes);
+      }
+    }
+  }
+}
+
+// TMA mode for pages shorter than a tile (page_size < 128, so a tile spans
+// several pages): the whole loader warp.  Lane l < 8 owns the tile's 16-key
+// block l, which never straddles a page (page sizes are multiples of 16), and
+// issues its two 16-slot boxes (row bytes 0-127 and 128-255 of the fill), so
+// the eight pieces of a tile are issued by one warp instruction instead of
+// one after another by a single thread.  Each lane loads its block's page id
+// a tile ahead.  Lane 0 waits for the staging tile and arrives with the byte
+// total once the warp has issued.
+template <class Fmt>
+__device__ __forceinline__ void role_loader_tma_blocks(const SplitArgs& a, Misc& M, bool is_v, uint8_t* stage,
+                                                       int lane) {
+  constexpr int kBlocks = kTileKeys / 16;
+  const CUtensorMap* map16 = (is_v ? a.v_maps : a.k_maps) + 3;  // boxes of 16 slots
+  uint64_t* full = is_v ? &M.vst_full : &M.kst_full;
+  uint64_t* empty = is_v ? &M.vst_empty : &M.kst_empty;
+  WaitCtl* abort = &M.ctl;
+  const int ps = a.page_size;
+  const uint32_t dst = smem_u32(stage) + 16 * lane * 128;
+  const uint64_t once = l2_policy_evict_first();  // K and V are read once per call
+  uint32_t f = 0;  // fills issued
+  for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
+    const Item x = sched_item(M.sched, a.B, it);
+    const int32_t* bt = a.block_table + (size_t)x.b * a.mpr;
+    const int nt = tiles_of(x);
+    // first key of this lane's block of tile jl, and whether it holds split keys
+    auto block_key = [&](int jl) { return x.t0 + jl * kTileKeys + 16 * lane; };
+    auto block_live = [&](int jl) { return lane < kBlocks && jl < nt && block_key(jl) < x.t1; };
+    int pg_next = block_live(0) ? ld_page_id(bt + block_key(0) / ps) : -1;
+    for (int jl = 0; jl < nt; ++jl) {
+      const int pg = pg_next;
+      pg_next = block_live(jl + 1) ? ld_page_id(bt + block_key(jl + 1) / ps) : -1;
+      const bool live = block_live(jl);
+      const bool ok = live && (unsigned)pg < (unsigned)a.num_pages;
+      if (live && !ok) {
+        atomicOr(a.status, 0x1u);
+        atomicOr(a.bad + x.b, 1u);
+      }
+      const int slot = block_key(jl) % ps;
+      const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, ok)) * 16u * 256u;
+#pragma unroll
+      for (int h = 0; h < Fmt::kFills; ++h, ++f) {
+        int go = 1;
+        if (lane == 0) go = mbar_wait(empty, (f & 1) ^ 1, abort) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, go, 0) == 0) return;
+        if (ok) {
+          tma_load_4d_hint(dst, map16, 256 * h, x.g, slot, pg, full, once);
+          tma_load_4d_hint(dst + 16384, map16, 256 * h + 128, x.g, slot, pg, full, once);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       }
     }
   }
@@ -985,7 +1041,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   const int vq = warp == 0 ? 0 : warp == 8 ? 1 : warp == 2 ? 2 : warp == 10 ? 3 : -1;
   if (warp == 3 || warp == 9) {
     const bool is_v = warp == 9;
-    if constexpr (TMA) {
+    // TMA: 1 = one thread (pages of a tile or more), 2 = the warp (shorter
+    // pages); a separate instantiation each, so no kernel carries both
+    if constexpr (TMA == 2) {
+      role_loader_tma_blocks<Fmt>(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst), lane);
+    } else if constexpr (TMA == 1) {
       if (lane == 0) role_loader_tma<Fmt>(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst));
     } else {
       role_loader_cp<Fmt>(a, M, is_v, lane, sm + (is_v ? L::kOffVst : L::kOffKst));
@@ -1062,9 +1122,11 @@ cudaError_t launch_mode(const SplitArgs& a, int grid, cudaStream_t stream) {
 
 // One element format's launcher (each format's instantiations live in their
 // own translation unit, split_kv_<format>.cu, so they compile in parallel).
-#define PA_DEFINE_SPLIT_LAUNCHER(name, Fmt)                                                       \
-  cudaError_t name(const SplitArgs& a, int grid, cudaStream_t stream) {                           \
-    return a.use_tma ? launch_mode<Fmt, 1>(a, grid, stream) : launch_mode<Fmt, 0>(a, grid, stream); \
+#define PA_DEFINE_SPLIT_LAUNCHER(name, Fmt)                                          \
+  cudaError_t name(const SplitArgs& a, int grid, cudaStream_t stream) {              \
+    if (!a.use_tma) return launch_mode<Fmt, 0>(a, grid, stream);                     \
+    return a.page_size < kTileKeys ? launch_mode<Fmt, 2>(a, grid, stream)            \
+                                   : launch_mode<Fmt, 1>(a, grid, stream);           \
   }
 
 }  // namespace pa
