@@ -264,13 +264,24 @@ static int run(const problem_t* P, const int32_t* rows, int n_rows, double* out,
     for (int i = 0; i < n_rows; ++i)
       if (rows[i] < 0 || rows[i] >= total_rows) return -1;
   int failed = 0;
+#if ORACLE_MUTATION == 14
+  /* planted mistake: one scratch buffer shared by every thread */
+  double* shared_s = (double*)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+  double* shared_acc = (double*)malloc(sizeof(double) * (size_t)P->D);
+#endif
 #ifdef _OPENMP
   if (num_threads <= 0) num_threads = omp_get_max_threads();
 #pragma omp parallel num_threads(num_threads)
 #endif
   {
+    /* each thread owns its score and accumulator scratch */
+#if ORACLE_MUTATION == 14
+    double* s = shared_s;
+    double* acc = shared_acc;
+#else
     double* s = (double*)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
     double* acc = (double*)malloc(sizeof(double) * (size_t)P->D);
+#endif
     if (!s || !acc) {
 #ifdef _OPENMP
 #pragma omp atomic write
@@ -282,12 +293,23 @@ static int run(const problem_t* P, const int32_t* rows, int n_rows, double* out,
 #endif
       for (int i = 0; i < count; ++i) {
         int r = rows ? rows[i] : i;
+        /* the i-th requested row goes to slot i of out and lse */
+#if ORACLE_MUTATION == 13
+        attend_row(P, r, out + (size_t)r * P->D, lse + r, s, acc);
+#else
         attend_row(P, r, out + (size_t)i * P->D, lse + i, s, acc);
+#endif
       }
     }
+#if ORACLE_MUTATION != 14
     free(s);
     free(acc);
+#endif
   }
+#if ORACLE_MUTATION == 14
+  free(shared_s);
+  free(shared_acc);
+#endif
   return failed ? -2 : 0;
 }
 

@@ -18,7 +18,10 @@ What pins what:
                         permuting pages together with the block table changes
                         nothing; zero-length rows are exact zeros even when Q is
                         NaN; two keys give sigmoid weights; one-hot V rows expose
-                        exactly which keys each verify query sees.
+                        exactly which keys each verify query sees;
+  * row selection     - any list of rows (shuffled, repeated) on any number of
+                        threads equals, bit for bit, the same rows of a
+                        one-thread evaluation of all rows.
 """
 from __future__ import annotations
 
@@ -291,7 +294,42 @@ def pin_causal_window(lib):
     return fails
 
 
+def pin_row_selection_and_threads(lib):
+    """Selected rows (shuffled, with repeats) and several threads give, bit
+    for bit, the rows of a one-thread evaluation of every row.  Each row is
+    one sequential evaluation of the definition, so neither the row order nor
+    the thread count may change a bit; this ties the i-th output slot to the
+    i-th requested row and keeps each thread's scratch its own."""
+    fails = []
+    cases = (
+        ("tiny", _tiny("fp8", 81, [37, 5, 2, 0], Hkv=2, group=3, q_len=4)),
+        ("medium", _tiny("fp8", 82, [1500, 700, 0, 9], Hkv=2, group=3, q_len=8, page_size=32)),
+        ("medium bf16", _tiny("bf16", 83, [900, 1200], Hkv=2, group=4, q_len=1, page_size=16)),
+    )
+    for name, w in cases:
+        s = w.spec
+        full, full_lse = run_oracle(w, lib=lib, num_threads=1)
+        flat = full.reshape(-1, s.head_dim)
+        flat_lse = full_lse.reshape(-1)
+        n = flat.shape[0]
+        rng = np.random.default_rng(7)
+        rows = np.concatenate([rng.permutation(n), rng.integers(0, n, n // 2 + 3)]).astype(np.int32)
+        rng.shuffle(rows)
+        for threads in (2, max(2, oracle.max_threads(lib))):
+            got, glse = run_oracle(w, rows=rows, lib=lib, num_threads=threads)
+            if got.shape != (rows.size, s.head_dim) or glse.shape != (rows.size,):
+                fails.append(f"{name}: row selection returned shapes {got.shape}, {glse.shape}")
+                continue
+            bad = ~((got == flat[rows]) | (np.isnan(got) & np.isnan(flat[rows]))).all(axis=1)
+            bad |= ~((glse == flat_lse[rows]) | (np.isnan(glse) & np.isnan(flat_lse[rows])))
+            if bad.any():
+                i = int(np.flatnonzero(bad)[0])
+                fails.append(f"{name}, {threads} threads: {int(bad.sum())} of {rows.size} selected rows differ "
+                             f"from the one-thread rows, first slot {i} (row {int(rows[i])})")
+    return fails
+
+
 ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_e5m2_vs_torch, pin_e5m2_closed_form,
             pin_e5m2_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
             pin_bruteforce_fp8, pin_bruteforce_e5m2, pin_bruteforce_bf16, pin_bruteforce_f16, pin_uniform_mean, pin_single_key, pin_permutation,
-            pin_zero_length, pin_two_key, pin_causal_window]
+            pin_zero_length, pin_two_key, pin_causal_window, pin_row_selection_and_threads]

@@ -30,6 +30,8 @@ MUTATIONS = {
     10: "lse without the max term",
     11: "E5M2 exponent bias 16",
     12: "E5M2 subnormals decoded as normals",
+    13: "selected row written to the slot of its row index instead of its list position",
+    14: "one score / accumulator scratch shared by every thread",
 }
 
 
