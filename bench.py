@@ -10,8 +10,12 @@ Printed JSON (one line, rank 0):
   value      effective KV GB/s = unique KV bytes of all steps on all ranks / max
              wall time over ranks (CUDA events, inputs resident in HBM)
   roofline   split-kernel achieved GB/s (algorithmic unique KV bytes / its own
-             average launch time, from CUDA events around every --timing-every-th
-             launch of the timed region) vs the measured HBM copy bandwidth
+             average launch time) vs the measured HBM copy bandwidth; the
+             launch time comes from CUDA events around each split-kernel launch
+             of a dedicated burst of --roofline-launches calls right after the
+             timed region (events between the split kernel and the combine
+             would hold back the combine's early launch, so the timed region
+             itself carries none)
   e2e        the same metric through the C ABI with pinned host buffers: each
              step copies its inputs host->device and reads the output back
   cpu_baseline  the FP64 oracle on a bounded sample, on this host's cores
@@ -205,9 +209,21 @@ def cpu_baseline_sample(w_cpu, seconds_target=15.0):
 # --------------------------------------------------------------------- arms --
 
 def describe(spec) -> str:
-    return (f"B{spec.batch} x {spec.max_ctx_len}-token contexts, page {spec.page_size}, Hkv {spec.num_kv_heads}, "
+    if spec.ctx_range is not None:
+        lo, hi = spec.ctx_range
+        ctx = f"B{spec.batch} slots, contexts uniform in [{lo}, {hi}] (drawn per working set)"
+        extra = [f"{len(spec.zero_slots)} forced zero-length"] if spec.zero_slots else []
+        extra += [f"{len(spec.padded_slots)} padded slots"] if spec.padded_slots else []
+        if extra:
+            ctx += " with " + " and ".join(extra)
+    else:
+        ctx = f"B{spec.batch} x {spec.max_ctx_len}-token contexts"
+    layout = ""
+    if spec.layout == "interleaved":
+        layout = ", K/V interleaved per token and head" + (f" at base + {spec.base_pad} B" if spec.base_pad else "")
+    return (f"{ctx}, page {spec.page_size}, Hkv {spec.num_kv_heads}, "
             f"Hq {spec.num_q_heads} (GQA {spec.num_q_heads // spec.num_kv_heads}), q_len {spec.q_len}, "
-            f"D {spec.head_dim}, " + KIND_TEXT[spec.kind] + ", random block table")
+            f"D {spec.head_dim}, " + KIND_TEXT[spec.kind] + layout + ", random block table")
 
 
 KIND_TEXT = {"fp8": "FP16 Q, E4M3 K/V per-tensor scales", "e5m2": "FP16 Q, E5M2 K/V per-tensor scales",
@@ -290,7 +306,8 @@ def run_gpu(args, dist, rank, world, local):
     nsets = args.working_sets
     sets = [wl.generate(spec, wl.working_set_seed(name, w) + 1000 * rank, device=dev) for w in range(nsets)]
     decs = [D.Decoder(w) for w in sets]
-    unique = sets[0].unique_kv_bytes()
+    uniq = [w.unique_kv_bytes() for w in sets]  # per working set (lengths may differ per set)
+    unique = uniq[0]
     stream = torch.cuda.current_stream(dev)
     for i in range(args.warmup):
         B.check(decs[i % nsets](stream), "warm-up call")
@@ -310,26 +327,27 @@ def run_gpu(args, dist, rank, world, local):
         dist.barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    every = max(1, args.timing_every)
     ev0.record(stream)
     for i in range(args.steps):
-        # per-launch events on a sample of the calls only: an event between
-        # the split kernel and the combine would hold back the combine's
-        # early (programmatic) launch on every call
-        sample = i % every == 0
-        if sample:
-            B.pa_timing_enable(True)
         B.check(decs[i % nsets](stream), "timed call")
-        if sample:
-            B.pa_timing_enable(False)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
     ms = ev0.elapsed_time(ev1)
+    timed_bytes = sum(uniq[i % nsets] for i in range(args.steps))
+    # roofline burst: the same calls back to back, CUDA events around every
+    # split-kernel (and combine) launch; a whole number of passes over the sets
+    n_roof = max(16, -(-args.roofline_launches // nsets) * nsets)
+    B.pa_timing_enable(True)
+    for i in range(n_roof):
+        B.check(decs[i % nsets](stream), "roofline call")
+    B.pa_timing_enable(False)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
     st0, split_ms, split_n = B.pa_timing_collect(0)
     st1, comb_ms, comb_n = B.pa_timing_collect(1)
+    roof_bytes = sum(uniq[i % nsets] for i in range(n_roof))
     for d in decs:
         if d.status() != 0:
             raise RuntimeError(f"status flags {d.status():#x} after the timed region")
@@ -377,14 +395,15 @@ def run_gpu(args, dist, rank, world, local):
         return
 
     peak, peak_kind = _peaks()
-    total_bytes = unique * args.steps * world
+    total_bytes = timed_bytes * world
     value = total_bytes / (ms / 1e3) / 1e9
     split_avg_s = split_ms / max(split_n, 1) / 1e3
-    achieved = unique / split_avg_s / 1e9
+    achieved = roof_bytes / max(split_n, 1) / split_avg_s / 1e9
     traffic = _traffic(name)
-    rotated = unique * nsets
-    l2_note = (f"no flush: every step's KV ({unique / 1e6:.0f} MB) exceeds the 129 MB L2" if unique > 129e6 else
-               f"no flush: {nsets} working sets of {unique / 1e6:.1f} MB rotated per call "
+    rotated = sum(uniq)
+    l2_note = (f"no flush: every step's KV ({min(uniq) / 1e6:.0f} MB or more) exceeds the 129 MB L2"
+               if min(uniq) > 129e6 else
+               f"no flush: {nsets} working sets of {min(uniq) / 1e6:.1f}-{max(uniq) / 1e6:.1f} MB rotated per call "
                f"({rotated / 1e6:.0f} MB in all)" + ("" if rotated > 129e6 else ", L2-resident: latency only"))
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -400,13 +419,16 @@ def run_gpu(args, dist, rank, world, local):
                    "global_batch": spec.batch * world, "seq_len": spec.max_ctx_len,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "working_sets": nsets, "l2": l2_note,
-                   "unique_kv_bytes_per_call": unique,
+                   "unique_kv_bytes_per_call": timed_bytes / args.steps,
                    "l2_bytes": int(getattr(props, "L2_cache_size", 0) or 0)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": f"split-KV kernel ({entry_point(spec)} main kernel)",
                      "kernel_avg_us": split_avg_s * 1e6, "combine_avg_us": comb_ms / max(comb_n, 1) * 1e3,
-                     "timed_launches": split_n},
+                     "timed_launches": split_n,
+                     "algorithmic_bytes_per_launch": roof_bytes / max(split_n, 1),
+                     "timing": f"CUDA events around each of {split_n} split-kernel launches of a burst of "
+                               f"{n_roof} calls after the timed region"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "e2e": {"value": unique * e_steps * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -429,8 +451,9 @@ def main():
     ap.add_argument("--working-sets", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--timing-every", type=int, default=8,
-                    help="per-launch CUDA events around every N-th timed call (roofline kernel time)")
+    ap.add_argument("--roofline-launches", type=int, default=64,
+                    help="calls in the roofline burst after the timed region (at least 16; CUDA events around "
+                         "each split-kernel launch)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

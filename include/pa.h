@@ -179,11 +179,17 @@ int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const 
  * cudaFree or allocating library routine).  Geometries whose workspace
  * (pa_decode_fp8_workspace_bytes) exceeds the array are rejected with
  * PA_ERR_WORKSPACE before anything is enqueued (B8 x 131072 keys, GQA 6,
- * q_len 8 needs 12.7 MB and fits).  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call on a device
- * shares the one array, which keeps the last call's contents; each call
- * clears the parts that must start at zero (status word, per-request flags).
+ * q_len 8 needs 12.7 MB and fits).  Every call looks up the array's device
+ * address (cudaGetSymbolAddress) in the current context.  The first call on a
+ * device is special: under CUDA's lazy module loading it is the lookup that
+ * loads the array's module, and the driver commits the 16 MiB at that moment,
+ * so that first call can block like an allocation.  Make one warm-up call per
+ * device at set-up, before any stream capture and before the latency-critical
+ * phase; from the second call on nothing is allocated or loaded.  Every call
+ * on a device shares the one array, which keeps the last call's contents;
+ * each call clears the parts that must start at zero (status word,
+ * per-request flags), so a bad input flagged by one call does not carry into
+ * the next.
  * Calls that overlap on the GPU (different streams, or several host threads)
  * race on the array and give undefined results: serialise them.  The status
  * word is cleared at the start of every call and cannot be read back.

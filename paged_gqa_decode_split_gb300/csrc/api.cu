@@ -262,21 +262,18 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
 // Scratch for pa_decode_fp8_noalloc: a module-scope device array that every
 // device loading this library holds until the process exits.  Host code must
 // not use its name as an address; the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress with the calling device current.  It is looked up on
+// every call rather than cached: the address belongs to the current context,
+// and a cached value would outlive a cudaDeviceReset or a switch to another
+// context on the same device.  Once the array's module is loaded the lookup
+// is a table search in the runtime and allocates nothing.
 constexpr size_t kNoallocScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-int noalloc_scratch(int dev, void** out) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {nullptr};
-  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+int noalloc_scratch(void** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+  *out = p;
   return PA_OK;
 }
 
@@ -347,10 +344,8 @@ int pa_decode_fp8_noalloc(const pa_params* p, const void* q, const void* k_pages
   const int st = check_geometry(p, 256, &R);
   if (st != PA_OK) return st;
   if (workspace_bytes(p, 256) > kNoallocScratchBytes) return PA_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   void* scratch = nullptr;
-  const int sst = noalloc_scratch(dev, &scratch);
+  const int sst = noalloc_scratch(&scratch);
   if (sst != PA_OK) return sst;
   return decode_common(kKvE4m3, p, q, k_pages, v_pages, block_table, ctx_lens, k_scale, v_scale, out, nullptr,
                        scratch, kNoallocScratchBytes, stream, /*clear_status=*/true);

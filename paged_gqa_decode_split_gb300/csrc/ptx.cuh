@@ -72,6 +72,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCt
   }
 }
 
+// Teardown wait after an abort: the same phase test, bounded by the cycle
+// limit alone (the abort flag is already set, so mbar_wait would return at
+// once).  Used to let this thread's own bulk copies into shared memory land
+// before the CTA exits.  Returns false if the bound ran out.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, const WaitCtl* ctl) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > ctl->limit) return false;
+  }
+  return true;
+}
+
 // Arrive once and add `bytes` to the transaction count the current phase waits for.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");

@@ -337,7 +337,11 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
 #pragma unroll
           for (int k = 0; k < 4; ++k) pq[k] = pq_tile[k];
         }
-        if (!mbar_wait(empty, (f & 1) ^ 1, abort)) return;
+        if (!mbar_wait(empty, (f & 1) ^ 1, abort)) {
+          // fill f - 1 may still be landing: let it finish before the CTA exits
+          if (f > 0) mbar_drain(full, (f - 1) & 1, abort);
+          return;
+        }
         uint32_t bytes = 0;
         bool bad = false;
         for (int r = 0; r < rows;) {
@@ -420,7 +424,11 @@ __device__ __forceinline__ void role_loader_tma_blocks(const SplitArgs& a, Misc&
 #pragma unroll
       for (int h = 0; h < Fmt::kFills; ++h, ++f) {
         int go = 1;
-        if (lane == 0) go = mbar_wait(empty, (f & 1) ^ 1, abort) ? 1 : 0;
+        if (lane == 0) {
+          go = mbar_wait(empty, (f & 1) ^ 1, abort) ? 1 : 0;
+          // fill f - 1 may still be landing: let it finish before the CTA exits
+          if (!go && f > 0) mbar_drain(full, (f - 1) & 1, abort);
+        }
         if (__shfl_sync(0xffffffffu, go, 0) == 0) return;
         if (ok) {
           tma_load_4d_hint(dst, map16, 256 * h, x.g, slot, pg, full, once);
@@ -572,6 +580,8 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
     }
     if (lane == 0) {
       ok = mbar_wait(&M.q_full, n & 1, abort);
+      // an abort while this item's Q boxes are in flight: let them land
+      if (!ok && a.q_tma && !a.withhold_q) mbar_drain(&M.q_full, n & 1, abort);
       for (int jl = 0; ok && jl < nt; ++jl, ++j) {
         if (j >= 2) ok = mbar_wait(&M.p_full[(j - 2) % kPBufs], ((j - 2) / kPBufs) & 1, abort);
         ok = ok && mbar_wait(&M.kbuf_full[j & 1], (j >> 1) & 1, abort);
