@@ -1,6 +1,7 @@
 """Benchmark: paged GQA verify-decode attention, B8 x 131072 keys, E4M3 K/V.
 
-One step = one pa_decode_fp8 call (split-KV kernel + log-sum-exp combine) over
+One step = one pa_decode_fp8 call (one kernel: split-KV attention, then the
+log-sum-exp merge of the split partials into the output rows) over
 one batch: 8 requests, 131072-token contexts, page 1648, 1 KV head, GQA 6,
 q_len 8, head_dim 256, FP16 Q, E4M3 K/V with per-tensor FP32 scales.  Steps
 rotate over 16 per-layer KV working sets (536,870,912 unique KV bytes each, so
@@ -9,13 +10,11 @@ every step's inputs are far larger than the 129 MB L2; no flush is needed).
 Printed JSON (one line, rank 0):
   value      effective KV GB/s = unique KV bytes of all steps on all ranks / max
              wall time over ranks (CUDA events, inputs resident in HBM)
-  roofline   split-kernel achieved GB/s (algorithmic unique KV bytes / its own
+  roofline   decode-kernel achieved GB/s (algorithmic unique KV bytes / its own
              average launch time) vs the measured HBM copy bandwidth; the
-             launch time comes from CUDA events around each split-kernel launch
-             of a dedicated burst of --roofline-launches calls right after the
-             timed region (events between the split kernel and the combine
-             would hold back the combine's early launch, so the timed region
-             itself carries none)
+             launch time comes from CUDA events around each kernel launch of a
+             dedicated burst of --roofline-launches calls right after the timed
+             region (the timed region itself carries no per-launch events)
   e2e        the same metric through the C ABI with pinned host buffers: each
              step copies its inputs host->device and reads the output back
   cpu_baseline  the FP64 oracle on a bounded sample, on this host's cores
@@ -337,7 +336,7 @@ def run_gpu(args, dist, rank, world, local):
     ms = ev0.elapsed_time(ev1)
     timed_bytes = sum(uniq[i % nsets] for i in range(args.steps))
     # roofline burst: the same calls back to back, CUDA events around every
-    # split-kernel (and combine) launch; a whole number of passes over the sets
+    # kernel launch; a whole number of passes over the sets
     n_roof = max(16, -(-args.roofline_launches // nsets) * nsets)
     B.pa_timing_enable(True)
     for i in range(n_roof):
@@ -346,7 +345,6 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     st0, split_ms, split_n = B.pa_timing_collect(0)
-    st1, comb_ms, comb_n = B.pa_timing_collect(1)
     roof_bytes = sum(uniq[i % nsets] for i in range(n_roof))
     for d in decs:
         if d.status() != 0:
@@ -423,13 +421,13 @@ def run_gpu(args, dist, rank, world, local):
                    "l2_bytes": int(getattr(props, "L2_cache_size", 0) or 0)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": f"split-KV kernel ({entry_point(spec)} main kernel)",
-                     "kernel_avg_us": split_avg_s * 1e6, "combine_avg_us": comb_ms / max(comb_n, 1) * 1e3,
+                     "kernel": f"split-KV kernel with its merge phase (the one kernel of {entry_point(spec)})",
+                     "kernel_avg_us": split_avg_s * 1e6,
                      "timed_launches": split_n,
                      "algorithmic_bytes_per_launch": roof_bytes / max(split_n, 1),
-                     "timing": f"CUDA events around each of {split_n} split-kernel launches of a burst of "
+                     "timing": f"CUDA events around each of {split_n} kernel launches of a burst of "
                                f"{n_roof} calls after the timed region"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": {"value": unique * e_steps * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
@@ -453,7 +451,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roofline-launches", type=int, default=64,
                     help="calls in the roofline burst after the timed region (at least 16; CUDA events around "
-                         "each split-kernel launch)")
+                         "each kernel launch)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -38,7 +38,8 @@
  * launcher", vllm.cpp pull request #48, description: KV is read once per
  * group).  Long contexts are cut into splits whose count depends only on that
  * request's length; each split writes FP32 (m, l, O) partials into the
- * request-major workspace and a log-sum-exp combine merges them in ascending
+ * request-major workspace and a log-sum-exp merge (the last phase of the same
+ * kernel, once every split of the request has arrived) combines them in ascending
  * split order ("DFlash2 concurrent long-context attention", same section:
  * independent request-major workspace panels).  Results therefore do not
  * depend on batch composition: a batched call writes, bit for bit, what one
@@ -350,11 +351,13 @@ int pa_debug_stall_next(int64_t wait_limit_cycles);
 
 /* ---- kernel timing ------------------------------------------------------------
  * pa_timing_enable(1) makes every later decode call record CUDA events around
- * its split-KV kernel and its combine kernel (on the call's stream);
- * pa_timing_collect synchronises those events and returns, for kernel
- * 0 = split-KV and 1 = combine, the summed device time in milliseconds and
- * the number of launches timed since the previous collect, then resets them.
- * Recording stops while disabled.  At most 4096 launches are kept. */
+ * its kernel (on the call's stream; one kernel per call: split-KV attention
+ * followed by the log-sum-exp merge of the split partials).
+ * pa_timing_collect synchronises those events and returns, for kernel 0 (the
+ * decode kernel), the summed device time in milliseconds and the number of
+ * launches timed since the previous collect, then resets them; kernel 1 is
+ * kept for compatibility and reports no launches.  Recording stops while
+ * disabled.  At most 4096 launches are kept. */
 int pa_timing_enable(int on);
 int pa_timing_collect(int kernel, double* total_ms, int64_t* launches);
 

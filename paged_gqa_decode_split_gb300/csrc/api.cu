@@ -114,6 +114,29 @@ bool encode_kv_map(CUtensorMap* m, const void* base, const pa_params* p, bool v,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D byte view of K or V: (row byte 0..127, KV head, slot, 128-byte part of
+// the key row, page), one box of 128 bytes x 1 head x 128 slots x 2 parts,
+// 128-byte swizzle.  The box lands as part 0 of its 128 slots, then part 1:
+// a whole staging tile of the split kernel in one copy.  Used only for tiles
+// inside one page (page_size >= 128).
+bool encode_kv_tile_map(CUtensorMap* m, const void* base, const pa_params* p, bool v, int row_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const long long hs = v ? p->v_head_stride : p->k_head_stride;
+  const long long ts = v ? p->v_token_stride : p->k_token_stride;
+  const long long ps = v ? p->v_page_stride : p->k_page_stride;
+  cuuint64_t dims[5] = {128, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size, (cuuint64_t)(row_bytes / 128),
+                        (cuuint64_t)p->num_pages};
+  cuuint64_t strides[4] = {(cuuint64_t)(p->num_kv_heads == 1 ? row_bytes : hs), (cuuint64_t)ts, 128, (cuuint64_t)ps};
+  cuuint32_t box[5] = {128, 1, (cuuint32_t)(p->page_size < 128 ? p->page_size : 128), 2, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  for (cuuint64_t s : strides)
+    if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D element view of Q [B][q_len][Hq][D] (16-bit elements): (d, query head,
 // verify query, request), boxes of 64 elements x G heads x q_len queries,
 // 128-byte swizzle.  One box is one 64-column atom of an item's packed Q tile,
@@ -173,7 +196,6 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
                   void* out, float* lse, void* workspace, size_t workspace_bytes_given, void* stream_ptr,
                   bool clear_status = false) {
   const bool scaled = fmt == kKvE4m3 || fmt == kKvE5m2;  // 8-bit K/V with FP32 per-tensor scales
-  const bool bf16_out = fmt == kKvBf16 || fmt == kKvBf16D256;
   const int D = fmt == kKvBf16 ? 128 : 256;
   const int row_bytes = D * (scaled ? 1 : 2);
   int R = 0;
@@ -198,7 +220,8 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* bad = reinterpret_cast<uint32_t*>(ws + kWsBadOff);
-  if (cudaMemsetAsync(bad, 0, sizeof(uint32_t) * p->batch, stream) != cudaSuccess) return PA_ERR_CUDA;
+  // per-request flags, split arrival counters and the merge-task counter start at zero
+  if (cudaMemsetAsync(bad, 0, kWsClearBytes, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (clear_status && cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return PA_ERR_CUDA;
 
   SplitArgs a;
@@ -209,10 +232,15 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.block_table = block_table;
   a.ctx_lens = ctx_lens;
   a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.panel_ml = reinterpret_cast<float2*>(ws + L.ml_off);
   a.panel_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.out = out;
+  a.lse = lse;
   a.status = status;
   a.bad = bad;
+  a.arrive = reinterpret_cast<uint32_t*>(ws + kWsArriveOff);
+  a.queue = reinterpret_cast<uint32_t*>(ws + kWsQueueOff);
   a.k_ps = p->k_page_stride, a.k_ts = p->k_token_stride, a.k_hs = p->k_head_stride;
   a.v_ps = p->v_page_stride, a.v_ts = p->v_token_stride, a.v_hs = p->v_head_stride;
   a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;
@@ -225,6 +253,8 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
     a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots, row_bytes) &&
                 encode_kv_map(&a.v_maps[m], v_pages, p, true, slots, row_bytes);
   }
+  a.use_tma = a.use_tma && encode_kv_tile_map(&a.k_map_tile, k_pages, p, false, row_bytes) &&
+              encode_kv_tile_map(&a.v_map_tile, v_pages, p, true, row_bytes);
   // the packed Q tile by TMA together with K and V; with 8-byte aligned K/V
   // the kernel runs its per-lane copy paths for all three
   a.q_tma = a.use_tma && encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
@@ -232,28 +262,16 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;
 
+  // one CTA per SM at most; at least as many as split items, and enough that
+  // the merge phase's two workers per CTA take about one output row each
   const long long max_items = (long long)p->batch * p->num_kv_heads * (s_max > 0 ? s_max : 1);
-  const int grid = (int)(max_items < nsm ? max_items : nsm);
+  const long long merge_ctas = ((long long)p->batch * p->num_kv_heads * R + 1) / 2;
+  const long long want = max_items > merge_ctas ? max_items : merge_ctas;
+  const int grid = (int)(want < nsm ? want : nsm);
   cudaEvent_t e0, e1;
   timing_slot(0, &e0, &e1);
   if (e0) cudaEventRecord(e0, stream);
   if (launch_split(a, fmt, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
-  if (e1) cudaEventRecord(e1, stream);
-
-  CombineArgs c;
-  c.ctx_lens = ctx_lens;
-  c.panel_ml = a.panel_ml;
-  c.panel_o = a.panel_o;
-  c.bad = bad;
-  c.out_scale_ptr = scaled ? v_scale : nullptr;
-  c.out_scale_mul = 1.0f;
-  c.out = out;
-  c.lse = lse;
-  c.B = a.B, c.Hkv = a.Hkv, c.Hq = a.Hq, c.G = a.G, c.q_len = a.q_len, c.R = R, c.D = D;
-  c.max_ctx = a.max_ctx, c.s_max = s_max;
-  timing_slot(1, &e0, &e1);
-  if (e0) cudaEventRecord(e0, stream);
-  if (launch_combine(c, bf16_out, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (e1) cudaEventRecord(e1, stream);
   return PA_OK;
 }

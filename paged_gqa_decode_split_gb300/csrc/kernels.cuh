@@ -19,6 +19,11 @@ struct SplitArgs {
   // use_tma != 0 (16-byte aligned bases and strides)
   CUtensorMap k_maps[4];
   CUtensorMap v_maps[4];
+  // 5-D byte views (row byte 0..127, KV head, slot, 128-byte part of the key
+  // row, page) with one box of 128 slots x 2 parts: a whole staging tile (128
+  // keys x 256 row bytes) inside one page in one copy; filled with the above
+  CUtensorMap k_map_tile;
+  CUtensorMap v_map_tile;
   // 4-D element view of Q (d, query head, verify query, request) with boxes of
   // 64 elements x G heads x q_len queries (one 128-byte swizzled atom of the
   // packed tile); used when q_tma != 0
@@ -31,27 +36,21 @@ struct SplitArgs {
   const int32_t* block_table;  // [B][mpr]
   const int32_t* ctx_lens;     // [B]
   const float* k_scale;        // 8-bit K/V formats only (E4M3, E5M2)
+  const float* v_scale;        // 8-bit K/V formats only: the merged output is multiplied by *v_scale
   float2* panel_ml;            // (m in log2 units, l) per (item, row)
   float* panel_o;              // unnormalised O per (item, row, d); 8-bit paths: without v_scale
+  void* out;                   // FP16, or BF16 for the BF16 formats: [B][q_len][Hq][D]
+  float* lse;                  // nullable: natural-log LSE per output row
   uint32_t* status;
   uint32_t* bad;
+  uint32_t* arrive;            // per request: softmax-group arrivals of its finished split items
+  uint32_t* queue;             // next merge task
   long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
   int B, Hkv, Hq, G, q_len, R, page_size, mpr, num_pages, max_ctx, s_max;
   long long wait_limit;  // pipeline wait bound in cycles (0: default)
   int withhold_q;        // test hook: never signal the Q tile, so the MMA wait runs out
 };
 
-struct CombineArgs {
-  const int32_t* ctx_lens;
-  const float2* panel_ml;
-  const float* panel_o;
-  const uint32_t* bad;
-  const float* out_scale_ptr;  // nullable: output is multiplied by *out_scale_ptr * out_scale_mul
-  float out_scale_mul;
-  void* out;                   // FP16, or BF16 for the BF16 formats
-  float* lse;                  // nullable
-  int B, Hkv, Hq, G, q_len, R, D, max_ctx, s_max;
-};
 
 int split_smem_bytes();
 cudaError_t launch_split(const SplitArgs& a, KvFormat fmt, int grid, cudaStream_t stream);
@@ -61,7 +60,6 @@ cudaError_t launch_split_e5m2(const SplitArgs& a, int grid, cudaStream_t stream)
 cudaError_t launch_split_f16(const SplitArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_split_bf16_d128(const SplitArgs& a, int grid, cudaStream_t stream);
 cudaError_t launch_split_bf16_d256(const SplitArgs& a, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const CombineArgs& a, bool bf16_out, cudaStream_t stream);
 cudaError_t launch_debug_worklist(const int32_t* ctx_lens, int B, int Hkv, int max_ctx, int32_t* items,
                                   int32_t max_items, int32_t* count, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_debug_gather(const uint8_t* base, long long ps, long long ts, long long hs, const int32_t* bt,

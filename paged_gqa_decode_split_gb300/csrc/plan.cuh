@@ -47,8 +47,10 @@ __host__ __device__ inline int max_splits_for(int max_ctx_len) {
 
 // ------------------------------------------------------------ workspace --
 // [0, 4)          status word (PA_FLAG_* bits, sticky)
-// [512, 768)      per-request "bad input" flags (cleared by the host API each call)
-// [1024, ...)     panel_ml: float2 (m, l) [B][Hkv][S_max][R]
+// [512, 768)      per-request "bad input" flags            } cleared by the host
+// [768, 1024)     per-request split arrival counters        } API before every
+// [1024, 1028)    next combine task (the merge phase's queue) } call
+// [1280, ...)     panel_ml: float2 (m, l) [B][Hkv][S_max][R]
 // [...]           panel_o : float      [B][Hkv][S_max][R][D]   (unnormalised partial O)
 struct WsLayout {
   size_t ml_off, o_off, total;
@@ -56,12 +58,15 @@ struct WsLayout {
 __host__ __device__ inline WsLayout ws_layout(int B, int Hkv, int s_max, int R, int D) {
   WsLayout w;
   size_t items = (size_t)B * Hkv * (size_t)s_max * R;
-  w.ml_off = 1024;
+  w.ml_off = 1280;
   w.o_off = (w.ml_off + items * 8 + 255) / 256 * 256;
   w.total = (w.o_off + items * (size_t)D * 4 + 255) / 256 * 256;
   return w;
 }
-constexpr size_t kWsBadOff = 512;
+constexpr size_t kWsBadOff = 512;      // uint32 [kMaxBatch]
+constexpr size_t kWsArriveOff = 768;   // uint32 [kMaxBatch]
+constexpr size_t kWsQueueOff = 1024;   // uint32
+constexpr size_t kWsClearBytes = 768;  // bytes cleared from kWsBadOff on: flags, counters and queue
 
 // ------------------------------------------------------------- schedule --
 // Every CTA derives the same ordered item list from ctx_lens: requests sorted

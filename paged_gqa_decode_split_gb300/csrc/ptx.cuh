@@ -110,6 +110,17 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// 5-D tiled tensor load with an L2 cache policy, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void* map, int c0, int c1, int c2, int c3, int c4,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read once: its lines are the first to be evicted.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
@@ -127,6 +138,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 // FP32 store to global memory with an L2 cache policy.
 __device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy) : "memory");
+}
+
+// GPU-scope acquire load / release add of a counter in global memory (the
+// hand-off between CTAs of one grid).  A release is cumulative: stores of
+// other threads of the CTA ordered before it by a barrier are published too.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Prefetch of the cache line holding `p` into L2.

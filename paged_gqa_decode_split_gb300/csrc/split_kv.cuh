@@ -151,6 +151,11 @@ struct Misc {
   alignas(16) float mref[kMaxRows];  // read as float4
   alignas(16) float alpha[kMaxRows];
   alignas(16) float red[4][kMaxRows];
+  // merge phase: per worker (two of 256 threads) its task, the wait outcome,
+  // the split weights and their weighted row sum
+  int ctask[2], cok[2];
+  float cw[2][kMaxSplits];
+  float clsum[2];
   Sched sched;
 };
 static_assert(offsetof(Misc, mref) % 16 == 0, "mref is read with 16-byte loads");
@@ -292,11 +297,13 @@ __device__ __forceinline__ int ld_page_id(const int32_t* p) {
   return v;
 }
 
-// TMA mode (16-byte aligned bases and strides): one thread.  The tile's keys
-// are cut at page boundaries; each piece (a multiple of 16 slots inside one
-// page) is covered by boxes of 128, 64, 32 and 16 slots of the 4-D byte view
-// (row byte, KV head, slot, page), two boxes (row bytes 0-127 and 128-255)
-// per piece of slots, so a tile inside one page is two copies.  Completion is
+// TMA mode (16-byte aligned bases and strides): one thread.  A tile inside
+// one page is one copy: a box of the 5-D byte view (row byte 0..127, KV head,
+// slot, 128-byte part of the row, page) that writes both halves.  Otherwise
+// the tile's keys are cut at page boundaries; each piece (a multiple of 16
+// slots inside one page) is covered by boxes of 128, 64, 32 and 16 slots of
+// the 4-D byte view (row byte, KV head, slot, page), two boxes (row bytes
+// 0-127 and 128-255) per piece of slots.  Completion is
 // counted in bytes on the tile's full barrier; the thread arrives with the
 // byte total after issuing the copies.  Page ids are kept for the current
 // page index and the three after it, each loaded several pages ahead.  The
@@ -307,6 +314,7 @@ __device__ __forceinline__ int ld_page_id(const int32_t* p) {
 template <class Fmt>
 __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, bool is_v, uint8_t* stage) {
   const CUtensorMap* maps = is_v ? a.v_maps : a.k_maps;  // boxes of 128, 64, 32, 16 slots
+  const CUtensorMap* tile_map = is_v ? &a.v_map_tile : &a.k_map_tile;  // 128 slots x both parts
   uint64_t* full = is_v ? &M.vst_full : &M.kst_full;
   uint64_t* empty = is_v ? &M.vst_empty : &M.kst_empty;
   WaitCtl* abort = &M.ctl;
@@ -355,7 +363,11 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
             pq[3] = q_cur + 3 <= q_last ? ld_page_id(bt + q_cur + 3) : -1;
           }
           const int pg = pq[0];
-          if ((unsigned)pg < (unsigned)a.num_pages) {
+          if ((unsigned)pg < (unsigned)a.num_pages && len == kTileKeys) {
+            // the whole tile inside one page: one box writes both parts
+            tma_load_5d_hint(dst_base, tile_map, 0, x.g, slot, 2 * h, pg, full, once);
+            bytes += kTileKeys * 256;
+          } else if ((unsigned)pg < (unsigned)a.num_pages) {
             int rr = r, sl = slot, left = len;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -991,10 +1003,125 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
       if (lane == 0) mbar_arrive(&M.o_free);
     }
     named_bar_sync(bar_id, 128);  // every warp of the group is done with mref and red
+    // the group's partials of this item are stored: one more arrival for the
+    // request (a release, cumulative over the group's stores before the barrier)
+    if (gt == 0) red_release_add_u32(a.arrive + x.b, 1u);
     if (gt < RG) M.mref[row0 + gt] = kNoMax;
     named_bar_sync(bar_id, 128);
   }
 }
+
+// Merge phase (after the CTA's own items): log-sum-exp combine of the split
+// partials into the output rows ("perf(fa2): port decode GQA group-swap into
+// d128 varlen launcher", vllm.cpp pull request #48: with num_splits > 1 the
+// split partials are merged by their log-sum-exp).  For one output row
+// (request b, KV head g, packed row r = qi * G + hl) with splits s = 0 .. S-1:
+//   M = max_s m_s,  w_s = 2^(m_s - M),  out = scale * sum_s w_s O_s / sum_s w_s l_s
+// with m in log2 units, the sum over s in ascending order and the weights'
+// sum by a fixed reduction tree, so the bits depend on S alone (batch
+// invariance).  A row with no visible key (M = -inf), a request of length 0
+// and a request flagged by an input check write +0.0.
+// Tasks are the rows of every (request, KV head) in schedule order, handed
+// out by a counter in the workspace to two workers of 256 threads (one
+// thread per d).  A task waits, bounded, until every split item of its request
+// has arrived (two softmax groups per item); each CTA's items are done before
+// it takes a task, and the launch is cooperative, so every item is being
+// worked on by a resident CTA.
+template <class Fmt>
+__device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid) {
+  const int w = tid >> 8;
+  if (w >= 2) return;  // threads 512..639 take no tasks
+  const int d = tid & 255;
+  const int bar = 3 + w;  // named barriers 3 and 4
+  const int per_req = a.Hkv * a.R;
+  const int total = a.B * per_req;
+  const float scale = Fmt::kElemBytes == 1 ? __ldg(a.v_scale) : 1.0f;
+  while (true) {
+    if (d == 0) M.ctask[w] = atomicAdd(a.queue, 1u);
+    named_bar_sync(bar, 256);
+    const int t = M.ctask[w];
+    if (t >= total) break;
+    const int b = M.sched.order[t / per_req];
+    const int g = (t % per_req) / a.R, row = t % a.R;
+    int ns = M.sched.nsplit[b];
+    if (d == 0) {
+      const uint32_t want = 2u * (uint32_t)ns * (uint32_t)a.Hkv;
+      const long long t0 = clock64();
+      int ok = 1;
+      while (ld_acquire_u32(a.arrive + b) < want) {
+        if (clock64() - t0 > M.ctl.limit) {
+          ok = 0;
+          break;
+        }
+      }
+      M.cok[w] = ok;
+    }
+    named_bar_sync(bar, 256);
+    if (!M.cok[w]) {
+      if (d == 0) atomicOr(a.status, 0x4u);
+      break;
+    }
+    if (__ldcg(a.bad + b) != 0u) ns = 0;
+    const int qi = row / a.G, hl = row % a.G;
+    const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
+    const size_t prow = (size_t)(b * a.Hkv + g) * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
+    // the partial O of every split, requested before the weights are known so
+    // that the two rounds of loads overlap
+    const float* o0 = a.panel_o + prow * Fmt::D;
+    const size_t sstride = (size_t)a.R * Fmt::D;
+    float o[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) o[s] = (s < ns && d < Fmt::D) ? __ldcg(o0 + s * sstride + d) : 0.f;
+    // one warp, splits s and s + 32 on lane s: M = max_s m_s, w_s = 2^(m_s - M),
+    // lsum = sum_s w_s l_s (a fixed reduction tree, so the bits depend on ns only)
+    if (d < 32) {
+      const int s = d;
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      if (s < ns) {
+        const float2 ml = __ldcg(a.panel_ml + prow + (size_t)s * a.R);
+        m0 = ml.x, l0 = ml.y;
+      }
+      if (s + 32 < ns) {
+        const float2 ml = __ldcg(a.panel_ml + prow + (size_t)(s + 32) * a.R);
+        m1 = ml.x, l1 = ml.y;
+      }
+      float Mx = fmaxf(m0, m1);
+#pragma unroll
+      for (int k = 16; k > 0; k >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, k));
+      const float w0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - Mx);
+      const float w1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - Mx);
+      float ls = w0 * l0 + w1 * l1;
+#pragma unroll
+      for (int k = 16; k > 0; k >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, k);
+      if (s < kMaxSplits) M.cw[w][s] = w0;
+      if (s + 32 < kMaxSplits) M.cw[w][s + 32] = w1;
+      if (s == 0) {
+        M.clsum[w] = ls;
+        if (a.lse != nullptr)
+          a.lse[orow] = (Mx == -INFINITY || !(ls > 0.f)) ? -INFINITY : (Mx + log2f(ls)) * 0.6931471805599453f;
+      }
+    }
+    named_bar_sync(bar, 256);
+    const float lsum = M.clsum[w];
+    if (d < Fmt::D) {
+      float val = 0.f;
+      if (lsum > 0.f) {
+        // accumulation in ascending split order
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(M.cw[w][s], o[s], acc) : acc;
+        val = acc / lsum * scale;
+      }
+      if constexpr (Fmt::kQBf16) {
+        reinterpret_cast<__nv_bfloat16*>(a.out)[orow * Fmt::D + d] = __float2bfloat16_rn(val);
+      } else {
+        reinterpret_cast<__half*>(a.out)[orow * Fmt::D + d] = __float2half_rn(val);
+      }
+    }
+    named_bar_sync(bar, 256);  // the worker's weights are read before the next task overwrites them
+  }
+}
+
 
 template <class Fmt, int NM, int TMA>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitArgs a) {
@@ -1040,9 +1167,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = M.tmem_base;
-  // the combine kernel may be launched now; it waits for this grid to finish
-  // before it reads anything this grid writes
-  asm volatile("griddepcontrol.launch_dependents;");
 
   // warp w runs on sub-partition w % 4; the TMEM lane quarter of the K decode
   // and softmax warps is w % 4 as well.  The V decode warps, the heaviest
@@ -1094,7 +1218,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tb, 512);
   }
-  if (tid == 0 && M.ctl.abort) atomicOr(a.status, 0x4u);
+  if (M.ctl.abort) {
+    if (tid == 0) atomicOr(a.status, 0x4u);
+    return;  // the call's output is invalid; other CTAs' merge waits run out
+  }
+  merge_phase<Fmt>(a, M, tid);
 }
 
 template <class Fmt, int NM, int TMA>
@@ -1113,8 +1241,19 @@ cudaError_t launch_one(const SplitArgs& a, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     set_on_devices.fetch_or(bit);
   }
-  kern<<<grid, kThreads, kSmem, stream>>>(a);
-  return cudaGetLastError();
+  // cooperative: the merge phase waits for split items of other CTAs, so
+  // every CTA of the grid must be resident at once (one per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <class Fmt, int TMA>
