@@ -263,9 +263,10 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.withhold_q = stall > 0 ? 1 : 0;
 
   // one CTA per SM at most; at least as many as split items, and enough that
-  // the merge phase's two workers per CTA take about one output row each
+  // the merge phase's five workers per CTA take about one task (128 output
+  // elements) each
   const long long max_items = (long long)p->batch * p->num_kv_heads * (s_max > 0 ? s_max : 1);
-  const long long merge_ctas = ((long long)p->batch * p->num_kv_heads * R + 1) / 2;
+  const long long merge_ctas = ((long long)p->batch * p->num_kv_heads * R * (D / 128) + 4) / 5;
   const long long want = max_items > merge_ctas ? max_items : merge_ctas;
   const int grid = (int)(want < nsm ? want : nsm);
   cudaEvent_t e0, e1;

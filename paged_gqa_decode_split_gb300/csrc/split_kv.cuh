@@ -151,11 +151,11 @@ struct Misc {
   alignas(16) float mref[kMaxRows];  // read as float4
   alignas(16) float alpha[kMaxRows];
   alignas(16) float red[4][kMaxRows];
-  // merge phase: per worker (two of 256 threads) its task, the wait outcome,
+  // merge phase: per worker (five of 128 threads) its task, the wait outcome,
   // the split weights and their weighted row sum
-  int ctask[2], cok[2];
-  float cw[2][kMaxSplits];
-  float clsum[2];
+  int ctask[5], cok[5];
+  float cw[5][kMaxSplits];
+  float clsum[5];
   Sched sched;
 };
 static_assert(offsetof(Misc, mref) % 16 == 0, "mref is read with 16-byte loads");
@@ -1021,30 +1021,36 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
 // sum by a fixed reduction tree, so the bits depend on S alone (batch
 // invariance).  A row with no visible key (M = -inf), a request of length 0
 // and a request flagged by an input check write +0.0.
-// Tasks are the rows of every (request, KV head) in schedule order, handed
-// out by a counter in the workspace to two workers of 256 threads (one
-// thread per d).  A task waits, bounded, until every split item of its request
-// has arrived (two softmax groups per item); each CTA's items are done before
-// it takes a task, and the launch is cooperative, so every item is being
-// worked on by a resident CTA.
+// A task is 128 consecutive elements d of one row (one thread per d); tasks
+// run over the rows of every (request, KV head) in schedule order and are
+// handed out by a counter in the workspace to five workers of 128 threads per
+// CTA.  A task waits, bounded, until every split item of its request has
+// arrived (two softmax groups per item); each CTA's items are done before it
+// takes a task, and the launch is cooperative, so every item is being worked
+// on by a resident CTA.
+constexpr int kMergeWorkers = kThreads / 128;
+static_assert(kMergeWorkers <= 5 && kMaxSplits <= 64, "merge worker state and weight layout");
+
 template <class Fmt>
 __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid) {
-  const int w = tid >> 8;
-  if (w >= 2) return;  // threads 512..639 take no tasks
-  const int d = tid & 255;
-  const int bar = 3 + w;  // named barriers 3 and 4
-  const int per_req = a.Hkv * a.R;
+  constexpr int kHalves = Fmt::D / 128;
+  const int w = tid >> 7;
+  const int e = tid & 127;
+  const int bar = 3 + w;  // named barriers 3 .. 3 + kMergeWorkers - 1
+  const int per_req = a.Hkv * a.R * kHalves;
   const int total = a.B * per_req;
   const float scale = Fmt::kElemBytes == 1 ? __ldg(a.v_scale) : 1.0f;
   while (true) {
-    if (d == 0) M.ctask[w] = atomicAdd(a.queue, 1u);
-    named_bar_sync(bar, 256);
+    if (e == 0) M.ctask[w] = atomicAdd(a.queue, 1u);
+    named_bar_sync(bar, 128);
     const int t = M.ctask[w];
     if (t >= total) break;
     const int b = M.sched.order[t / per_req];
-    const int g = (t % per_req) / a.R, row = t % a.R;
+    const int rr = (t % per_req) / kHalves;  // row of the request (KV head major)
+    const int g = rr / a.R, row = rr % a.R;
+    const int d = (t % kHalves) * 128 + e;
     int ns = M.sched.nsplit[b];
-    if (d == 0) {
+    if (e == 0) {
       const uint32_t want = 2u * (uint32_t)ns * (uint32_t)a.Hkv;
       const long long t0 = clock64();
       int ok = 1;
@@ -1056,9 +1062,9 @@ __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid
       }
       M.cok[w] = ok;
     }
-    named_bar_sync(bar, 256);
+    named_bar_sync(bar, 128);
     if (!M.cok[w]) {
-      if (d == 0) atomicOr(a.status, 0x4u);
+      if (e == 0) atomicOr(a.status, 0x4u);
       break;
     }
     if (__ldcg(a.bad + b) != 0u) ns = 0;
@@ -1067,15 +1073,15 @@ __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid
     const size_t prow = (size_t)(b * a.Hkv + g) * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
     // the partial O of every split, requested before the weights are known so
     // that the two rounds of loads overlap
-    const float* o0 = a.panel_o + prow * Fmt::D;
+    const float* o0 = a.panel_o + prow * Fmt::D + d;
     const size_t sstride = (size_t)a.R * Fmt::D;
     float o[kMaxSplits];
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) o[s] = (s < ns && d < Fmt::D) ? __ldcg(o0 + s * sstride + d) : 0.f;
+    for (int s = 0; s < kMaxSplits; ++s) o[s] = s < ns ? __ldcg(o0 + s * sstride) : 0.f;
     // one warp, splits s and s + 32 on lane s: M = max_s m_s, w_s = 2^(m_s - M),
     // lsum = sum_s w_s l_s (a fixed reduction tree, so the bits depend on ns only)
-    if (d < 32) {
-      const int s = d;
+    if (e < 32) {
+      const int s = e;
       float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
       if (s < ns) {
         const float2 ml = __ldcg(a.panel_ml + prow + (size_t)s * a.R);
@@ -1097,31 +1103,28 @@ __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid
       if (s + 32 < kMaxSplits) M.cw[w][s + 32] = w1;
       if (s == 0) {
         M.clsum[w] = ls;
-        if (a.lse != nullptr)
+        if (a.lse != nullptr && d == 0)
           a.lse[orow] = (Mx == -INFINITY || !(ls > 0.f)) ? -INFINITY : (Mx + log2f(ls)) * 0.6931471805599453f;
       }
     }
-    named_bar_sync(bar, 256);
+    named_bar_sync(bar, 128);
     const float lsum = M.clsum[w];
-    if (d < Fmt::D) {
-      float val = 0.f;
-      if (lsum > 0.f) {
-        // accumulation in ascending split order
-        float acc = 0.f;
+    float val = 0.f;
+    if (lsum > 0.f) {
+      // accumulation in ascending split order
+      float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(M.cw[w][s], o[s], acc) : acc;
-        val = acc / lsum * scale;
-      }
-      if constexpr (Fmt::kQBf16) {
-        reinterpret_cast<__nv_bfloat16*>(a.out)[orow * Fmt::D + d] = __float2bfloat16_rn(val);
-      } else {
-        reinterpret_cast<__half*>(a.out)[orow * Fmt::D + d] = __float2half_rn(val);
-      }
+      for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(M.cw[w][s], o[s], acc) : acc;
+      val = acc / lsum * scale;
     }
-    named_bar_sync(bar, 256);  // the worker's weights are read before the next task overwrites them
+    if constexpr (Fmt::kQBf16) {
+      reinterpret_cast<__nv_bfloat16*>(a.out)[orow * Fmt::D + d] = __float2bfloat16_rn(val);
+    } else {
+      reinterpret_cast<__half*>(a.out)[orow * Fmt::D + d] = __float2half_rn(val);
+    }
+    named_bar_sync(bar, 128);  // the worker's weights are read before the next task overwrites them
   }
 }
-
 
 template <class Fmt, int NM, int TMA>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constant__ SplitArgs a) {
