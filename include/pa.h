@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 /* Return codes.  Every host-detectable problem is reported before any launch;
  * nothing is written to out, lse or workspace in that case. */
@@ -132,10 +132,15 @@ int pa_get_capabilities(pa_caps* out);
 const char* pa_status_string(int status);
 
 /* Host copy of the split planner the kernels run on the device: a request of
- * ctx_len keys is cut into *num_splits consecutive splits of *chunk keys (the
- * last one shorter).  Depends on ctx_len only, never on the batch.  ctx_len 0
- * gives 0 splits.  Returns PA_ERR_NULL or PA_ERR_SHAPE (ctx_len < 0). */
-int pa_split_plan(int32_t ctx_len, int32_t* num_splits, int32_t* chunk);
+ * ctx_len keys, read for each of num_kv_heads KV heads, is cut into
+ * *num_splits consecutive splits of *chunk keys (the last one shorter).
+ * Depends on ctx_len and num_kv_heads (the packed geometry, "perf(fa2): port
+ * decode GQA group-swap into d128 varlen launcher", vllm.cpp pull request
+ * #48: the split count is chosen on the packed geometry), never on the batch:
+ * about 512 * min(num_kv_heads, 4) keys per split, at most max_splits splits,
+ * whole 128-key tiles.  ctx_len 0 gives 0 splits.  Returns PA_ERR_NULL or
+ * PA_ERR_SHAPE (ctx_len < 0 or num_kv_heads < 1). */
+int pa_split_plan(int32_t ctx_len, int32_t num_kv_heads, int32_t* num_splits, int32_t* chunk);
 
 /* ---- FP16 Q x E4M3 K/V, head_dim 256 ---------------------------------------
  *

@@ -67,7 +67,7 @@ def load() -> ctypes.CDLL:
         sig = {
             "pa_get_capabilities": ([_P(pa_caps)], ctypes.c_int),
             "pa_status_string": ([ctypes.c_int], ctypes.c_char_p),
-            "pa_split_plan": ([i32, _P(i32), _P(i32)], ctypes.c_int),
+            "pa_split_plan": ([i32, i32, _P(i32), _P(i32)], ctypes.c_int),
             "pa_decode_fp8_workspace_bytes": ([pp], sz),
             "pa_decode_fp8": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_fp8_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
@@ -149,9 +149,9 @@ def pa_get_capabilities() -> pa_caps:
     return c
 
 
-def pa_split_plan(ctx_len: int) -> tuple[int, int, int]:
+def pa_split_plan(ctx_len: int, num_kv_heads: int = 1) -> tuple[int, int, int]:
     s, c = ctypes.c_int32(), ctypes.c_int32()
-    st = load().pa_split_plan(int(ctx_len), ctypes.byref(s), ctypes.byref(c))
+    st = load().pa_split_plan(int(ctx_len), int(num_kv_heads), ctypes.byref(s), ctypes.byref(c))
     return st, s.value, c.value
 
 

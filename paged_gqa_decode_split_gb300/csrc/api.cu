@@ -329,11 +329,11 @@ const char* pa_status_string(int status) {
   }
 }
 
-int pa_split_plan(int32_t ctx_len, int32_t* num_splits, int32_t* chunk) {
+int pa_split_plan(int32_t ctx_len, int32_t num_kv_heads, int32_t* num_splits, int32_t* chunk) {
   if (!num_splits || !chunk) return PA_ERR_NULL;
-  if (ctx_len < 0) return PA_ERR_SHAPE;
+  if (ctx_len < 0 || num_kv_heads < 1) return PA_ERR_SHAPE;
   int s, c;
-  split_plan(ctx_len, s, c);
+  split_plan(ctx_len, num_kv_heads, s, c);
   *num_splits = s;
   *chunk = c;
   return PA_OK;

@@ -9,7 +9,8 @@ namespace pa {
 
 // ------------------------------------------------------------ constants --
 constexpr int kTileKeys = 128;     // keys per tensor-core tile (MMA M dimension)
-constexpr int kSplitTarget = 512;  // a split holds about this many keys before the cap
+constexpr int kSplitTarget = 512;  // a split holds about this many keys per KV head factor before the cap
+constexpr int kMaxHeadFactor = 4;  // the split floor grows with the KV head count up to this factor
 constexpr int kMaxSplits = 38;     // at most this many splits per request: a quarter of the 152 SMs,
                                    // so 4, 8 or 16 long requests fill whole waves of a one-CTA-per-SM grid
 constexpr int kMaxBatch = 64;
@@ -19,26 +20,33 @@ constexpr int kMaxRows = 64;       // G * q_len rows of one packed tile
 constexpr int kPageMultiple = 16;
 constexpr int kMaxCtx = 1 << 20;
 
-// Split plan of one request of L keys.  It depends on L alone, never on the
-// batch, so a request produces the same partials (and the combine the same
-// bits) whether it runs alone or next to others.  Splits are whole tiles of
-// kTileKeys keys except the last; every split is non-empty.
-__host__ __device__ inline void split_plan(int L, int& num_splits, int& chunk) {
+// Split plan of one request of L keys over Hkv KV heads.  It depends on the
+// request's length and on the packed geometry (the KV head count), never on
+// the batch, so a request produces the same partials (and the merge the same
+// bits) whether it runs alone or next to others.  With several KV heads a
+// request already yields Hkv work items per split, so the split floor grows
+// with Hkv (up to kMaxHeadFactor): fewer, longer items, less per-item cost.
+// Splits are whole tiles of kTileKeys keys except the last; every split is
+// non-empty.
+__host__ __device__ inline void split_plan(int L, int Hkv, int& num_splits, int& chunk) {
   if (L <= 0) {
     num_splits = 0;
     chunk = 0;
     return;
   }
-  int s0 = (L + kSplitTarget - 1) / kSplitTarget;
+  const int f = Hkv < 1 ? 1 : (Hkv > kMaxHeadFactor ? kMaxHeadFactor : Hkv);
+  const int target = kSplitTarget * f;
+  int s0 = (L + target - 1) / target;
   s0 = s0 < 1 ? 1 : (s0 > kMaxSplits ? kMaxSplits : s0);
   int per = (L + s0 - 1) / s0;
   chunk = (per + kTileKeys - 1) / kTileKeys * kTileKeys;
   num_splits = (L + chunk - 1) / chunk;
 }
 
-// Upper bound of split_plan's count over every L <= max_ctx_len.  The count
-// itself is not monotone in L (the split length jumps by whole tiles), but it
-// never exceeds clamp(ceil(L / kSplitTarget), 1, kMaxSplits), which is.
+// Upper bound of split_plan's count over every L <= max_ctx_len and every
+// Hkv.  The count itself is not monotone in L (the split length jumps by
+// whole tiles), but it never exceeds clamp(ceil(L / kSplitTarget), 1,
+// kMaxSplits), which is (and which a larger head factor only lowers).
 __host__ __device__ inline int max_splits_for(int max_ctx_len) {
   if (max_ctx_len <= 0) return 1;
   int s0 = (max_ctx_len + kSplitTarget - 1) / kSplitTarget;
@@ -101,7 +109,7 @@ __device__ inline void sched_build(Sched& S, const int32_t* ctx_lens, int B, int
       L = 0;
     }
     int ns, ch;
-    split_plan(L, ns, ch);
+    split_plan(L, Hkv, ns, ch);
     S.len[t] = L;
     S.nsplit[t] = ns;
     S.chunk[t] = ch;

@@ -138,13 +138,14 @@ constexpr int kSoftmaxBar = 1;     // named barriers 1 and 2: the two softmax gr
 
 // TMEM column map (512 columns allocated)
 constexpr uint32_t kColS = 0;     // S^T, 2 buffers of 64 columns
-constexpr uint32_t kColO = 128;   // O^T, d 0..127 at +0, d 128..255 at +64
+constexpr uint32_t kColO = 128;   // O^T, d 0..127 at +0, d 128..255 at +64; head_dim 128: two buffers
+                                  // of 64 columns, item n in buffer n & 1 (its epilogue overlaps item n + 1)
 constexpr uint32_t kColK = 256;   // K' operand, 2 buffers of 128 columns
 
 struct Misc {
   uint64_t kst_full, kst_empty, vst_full, vst_empty;  // the K and V staging tiles
   uint64_t kbuf_full[2], s_full[2], vtile_full[2], p_full[kPBufs], pv_done[kPBufs];
-  uint64_t q_full, q_empty, o_free, fin, fin_qk;
+  uint64_t q_full, q_empty, o_free[2], fin, fin_qk;
   uint32_t tmem_base;
   WaitCtl ctl;
   alignas(16) int vote[2][2][4];     // per-warp vote words of each softmax group, double-buffered
@@ -269,6 +270,16 @@ __device__ __forceinline__ size_t panel_index(const SplitArgs& a, const Item& x)
 }
 
 __device__ __forceinline__ int tiles_of(const Item& x) { return (x.t1 - x.t0 + kTileKeys - 1) / kTileKeys; }
+
+// O^T buffers: one (head_dim 256 fills the 128 columns) or two of 64 columns
+// (head_dim 128), the CTA's n-th item in buffer n % kOBufs
+template <class Fmt>
+struct OBuf {
+  static constexpr int kBufs = Fmt::D == 128 ? 2 : 1;
+  static __device__ __forceinline__ uint32_t col(int n) { return kColO + 64u * (uint32_t)(n % kBufs); }
+  // the epilogue of item n - kBufs released buffer n % kBufs
+  static __device__ __forceinline__ uint32_t free_parity(int n) { return (uint32_t)((n / kBufs) & 1) ^ 1u; }
+};
 
 // ------------------------------------------------------------------ roles --
 
@@ -748,7 +759,7 @@ __device__ __forceinline__ void role_pv(const SplitArgs& a, Misc& M, uint32_t tb
     for (int jl = 0; jl < nt; ++jl, ++pj) {
       const uint32_t pb = pj % kPBufs, pu = pj / kPBufs;
       if (!mbar_wait(&M.p_full[pb], pu & 1, abort)) return;
-      if (jl == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, abort)) return;
+      if (jl == 0 && !mbar_wait(&M.o_free[n % OBuf<Fmt>::kBufs], OBuf<Fmt>::free_parity(n), abort)) return;
       if (!mbar_wait(&M.vtile_full[pj & 1], (pj >> 1) & 1, abort)) return;
       tc_fence_after();
       const uint64_t pd = sdesc_add(p_desc, pb * 16384);
@@ -761,7 +772,7 @@ __device__ __forceinline__ void role_pv(const SplitArgs& a, Misc& M, uint32_t tb
         for (int h = 0; h < kHalves; ++h) {
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
-            mma_ss(tb + kColO + 64 * h, sdesc_add(vd, 2 * h * L::kVAtom + kk * 2048),
+            mma_ss(tb + OBuf<Fmt>::col(n) + 64 * h, sdesc_add(vd, 2 * h * L::kVAtom + kk * 2048),
                    sdesc_add(pd, (2 * pq + kk) * 2048), id_pv, (pq == 0 && kk == 0) ? first : 1u);
         }
         slot = slot + 1 == L::kVSlots ? 0 : slot + 1;
@@ -826,9 +837,10 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
     tmem_wait_ld();
     reg_fence(r);
   };
-  for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
+  for (int it = blockIdx.x, n = 0; it < M.sched.total; it += gridDim.x, ++n) {
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
+    const uint32_t ocol = OBuf<Fmt>::col(n);  // this item's O^T columns
     const int lim = x.L - a.q_len;  // packed row r sees key t iff t <= lim + r / G
     float lsum[RG];                 // running row sums of this thread's key slot
 #pragma unroll
@@ -913,7 +925,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
 #pragma unroll
             for (int c = 0; c < RG / 8; ++c) {
               uint32_t r[8];
-              const uint32_t ta = lane_base + kColO + 64 * h + row0 + 8 * c;
+              const uint32_t ta = lane_base + ocol + 64 * h + row0 + 8 * c;
               PA_TMEM_LD_X8(ta, r);
               tmem_wait_ld();
               reg_fence(r);
@@ -974,10 +986,10 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
       // item's PV products, then the stores
       uint32_t r[kHalves][RG];
 #pragma unroll
-      for (int h = 0; h < kHalves; ++h) tmem_load_rows(lane_base + kColO + 64 * h + row0, r[h]);
+      for (int h = 0; h < kHalves; ++h) tmem_load_rows(lane_base + ocol + 64 * h + row0, r[h]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&M.o_free);
+      if (lane == 0) mbar_arrive(&M.o_free[n % OBuf<Fmt>::kBufs]);
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
 #pragma unroll
@@ -991,7 +1003,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
 #pragma unroll
       for (int h = 0; h < kHalves; ++h) {
         uint32_t r[RG];
-        tmem_load_rows(lane_base + kColO + 64 * h + row0, r);
+        tmem_load_rows(lane_base + ocol + 64 * h + row0, r);
 #pragma unroll
         for (int k = 0; k < RG; ++k) {
           const int row = row0 + k;
@@ -1000,7 +1012,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&M.o_free);
+      if (lane == 0) mbar_arrive(&M.o_free[n % OBuf<Fmt>::kBufs]);
     }
     named_bar_sync(bar_id, 128);  // every warp of the group is done with mref and red
     // the group's partials of this item are stored: one more arrival for the
@@ -1149,7 +1161,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     }
     mbar_init(&M.q_full, 1);
     mbar_init(&M.q_empty, 1);
-    mbar_init(&M.o_free, 8);
+    mbar_init(&M.o_free[0], 8);
+    mbar_init(&M.o_free[1], 8);
     mbar_init(&M.fin, 1);
     mbar_init(&M.fin_qk, 1);
     M.ctl.abort = 0;

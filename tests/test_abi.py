@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_capabilities(lib):
     c = B.pa_get_capabilities()
-    assert c.abi_version == 1
+    assert c.abi_version == 2
     assert c.accum_bits == 32
     assert c.page_multiple == 16
     assert c.fp8_head_dim == 256 and c.bf16_head_dim == 128
@@ -40,23 +40,24 @@ def test_status_strings(lib):
         assert isinstance(B.status_string(code), str) and B.status_string(code)
 
 
-def splits_for_len(L: int) -> tuple[int, int]:
-    """Restatement of the split policy: about 512 keys per split, at most 38
-    splits (a quarter of the 152 SMs), split length a whole number of 128-key
-    tiles."""
+def splits_for_len(L: int, hkv: int = 1) -> tuple[int, int]:
+    """Restatement of the split policy: about 512 * min(Hkv, 4) keys per
+    split, at most 38 splits (a quarter of the 152 SMs), split length a whole
+    number of 128-key tiles."""
     if L <= 0:
         return 0, 0
-    s0 = min(max(math.ceil(L / 512), 1), 38)
+    s0 = min(max(math.ceil(L / (512 * min(hkv, 4))), 1), 38)
     chunk = math.ceil(math.ceil(L / s0) / 128) * 128
     return math.ceil(L / chunk), chunk
 
 
+@pytest.mark.parametrize("hkv", [1, 2, 3, 8])
 @pytest.mark.parametrize("L", [0, 1, 7, 8, 127, 128, 129, 511, 512, 513, 3297, 16383, 32768, 131072, 131073,
                                200000, 262144, 1 << 20])
-def test_split_plan_matches_restatement(lib, L):
-    st, s, c = B.pa_split_plan(L)
+def test_split_plan_matches_restatement(lib, L, hkv):
+    st, s, c = B.pa_split_plan(L, hkv)
     assert st == 0
-    assert (s, c) == splits_for_len(L)
+    assert (s, c) == splits_for_len(L, hkv)
     if L > 0:
         assert 1 <= s <= 38 and c % 128 == 0
         assert (s - 1) * c < L <= s * c  # every split non-empty
@@ -70,7 +71,8 @@ def test_split_count_bounded_by_workspace_bound(lib):
     worst = 0
     for L in range(0, 70000, 7):
         worst = max(worst, B.pa_split_plan(L)[1])
-        assert B.pa_split_plan(L)[1] <= min(38, max(1, math.ceil(L / 512)))
+        for hkv in (1, 2, 4, 8):
+            assert B.pa_split_plan(L, hkv)[1] <= min(38, max(1, math.ceil(L / 512)))
     assert worst == 38
     # the workspace of max_ctx_len 19457 must hold 38 splits per (request, KV head)
     p = _params(max_ctx_len=19457, max_pages_per_req=12)
@@ -79,6 +81,7 @@ def test_split_count_bounded_by_workspace_bound(lib):
 
 def test_split_plan_rejects_negative(lib):
     assert B.pa_split_plan(-1)[0] == B.PA_ERR_SHAPE
+    assert B.pa_split_plan(100, 0)[0] == B.PA_ERR_SHAPE
 
 
 def test_split_plan_known_configs(lib):
@@ -86,6 +89,9 @@ def test_split_plan_known_configs(lib):
     assert B.pa_split_plan(32768)[1:] == (37, 896)
     assert B.pa_split_plan(3297)[1:] == (7, 512)
     assert B.pa_split_plan(262144)[1:] == (38, 6912)
+    # the head count stretches the split floor: 8 KV heads give splits of 2048 keys or more
+    assert B.pa_split_plan(16384, 8)[1:] == (8, 2048)
+    assert B.pa_split_plan(262144, 2)[1:] == (38, 6912)
 
 
 def _params(**kw):

@@ -302,7 +302,7 @@ def schedule(lens, Hkv):
     descending (ties by index), then KV head, then split."""
     plans = []
     for L in lens:
-        st, s, c = B.pa_split_plan(max(L, 0))
+        st, s, c = B.pa_split_plan(max(L, 0), Hkv)
         plans.append((s, c))
     order = sorted(range(len(lens)), key=lambda b: (-plans[b][1], b))
     items = []
