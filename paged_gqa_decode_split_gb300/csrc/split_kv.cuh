@@ -883,17 +883,21 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
           v[k + 3] = fmaf(v[k + 3], c_log2, -m.w);
         }
       };
+      // the item's first tile sets every row's reference max (it starts at
+      // kNoMax), so it skips the check: v keeps the raw scores for the max
       float v[RG];
       load_scores(v);
-      to_log2(v);
-      bool ex = false;
+      bool ex = jl == 0;
+      if (jl > 0) {
+        to_log2(v);
 #pragma unroll
-      for (int k = 0; k < RG; ++k) ex |= v[k] > kTau;
+        for (int k = 0; k < RG; ++k) ex |= v[k] > kTau;
+      }
       const int f = vote(ex);
       if (f & 2) return;
       if (f & 1) {
-        // tile max of the group's rows from the raw scores (reloaded)
-        load_scores(v);
+        // tile max of the group's rows from the raw scores (reloaded after a check)
+        if (jl > 0) load_scores(v);
         float mx[BF::Half];
         BF::template run_from<true>(v, mx, lane);
 #pragma unroll
@@ -936,7 +940,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
           }
           tmem_wait_st();
         }
-        load_scores(v);  // reloaded rather than held across the rescale
+        if (jl > 0) load_scores(v);  // reloaded rather than held across the rescale
         to_log2(v);
       }
       // probabilities with the (possibly moved) references -> the P^T row
