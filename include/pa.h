@@ -344,6 +344,21 @@ int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_p
                         const int32_t* block_table, const int32_t* ctx_lens, int32_t which, void* dst,
                         void* stream);
 
+/* pa_debug_kv_load_path writes to *path how a decode call with this geometry
+ * and these K/V base pointers moves K and V rows into shared memory:
+ *   1  TMA boxes: both bases and every stride 16-byte aligned;
+ *   2  TMA windows: both bases 8 bytes past a 16-byte boundary and every
+ *      stride a multiple of 16 (each key's 256 row bytes of a fill arrive in a
+ *      272-byte window that starts 8 bytes before them);
+ *   0  8-byte cp.async copies: any other 8-byte aligned layout, or a layout
+ *      whose tensor maps the CUDA driver refused to encode.
+ * head_dim is 128 or 256, elem_bytes the K/V element size (1 for E4M3/E5M2,
+ * 2 for FP16/BF16).  Nothing is launched; the pointers are not dereferenced.
+ * Returns PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_UNSUPPORTED (head_dim or
+ * elem_bytes) or PA_ERR_ALIGN (a base or stride not a multiple of 8). */
+int pa_debug_kv_load_path(const pa_params* p, int32_t head_dim, int32_t elem_bytes, const void* k_pages,
+                          const void* v_pages, int32_t* path);
+
 /* ---- wait-bound check --------------------------------------------------------
  * Test hook for the kernels' bounded waits.  The next pa_decode_* call made in
  * this process (by any thread) runs its split kernel with every pipeline wait

@@ -84,6 +84,7 @@ def load() -> ctypes.CDLL:
             "pa_clear_status": ([vp, vp], ctypes.c_int),
             "pa_debug_worklist": ([pp, vp, vp, i32, vp, vp], ctypes.c_int),
             "pa_debug_gather_fp8": ([pp, vp, vp, vp, vp, i32, vp, vp], ctypes.c_int),
+            "pa_debug_kv_load_path": ([pp, i32, i32, vp, vp, _P(i32)], ctypes.c_int),
             "pa_debug_stall_next": ([i64], ctypes.c_int),
             "pa_timing_enable": ([ctypes.c_int], ctypes.c_int),
             "pa_timing_collect": ([ctypes.c_int, _P(ctypes.c_double), _P(i64)], ctypes.c_int),
@@ -252,6 +253,18 @@ def pa_debug_worklist(p: pa_params, ctx_lens, items, max_items: int, count, stre
 def pa_debug_gather_fp8(p: pa_params, k_pages, v_pages, block_table, ctx_lens, which: int, dst, stream=None) -> int:
     return load().pa_debug_gather_fp8(ctypes.byref(p), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                       _ptr(ctx_lens), int(which), _ptr(dst), _stream(stream))
+
+
+PA_KV_LOAD_COPY, PA_KV_LOAD_TMA, PA_KV_LOAD_WINDOW = 0, 1, 2
+
+
+def pa_debug_kv_load_path(p: pa_params, head_dim: int, elem_bytes: int, k_pages, v_pages) -> tuple[int, int]:
+    """(status, path): how a decode call with this geometry and these K/V
+    bases loads K and V (PA_KV_LOAD_*)."""
+    path = ctypes.c_int32(-1)
+    st = load().pa_debug_kv_load_path(ctypes.byref(p), int(head_dim), int(elem_bytes), _ptr(k_pages),
+                                      _ptr(v_pages), ctypes.byref(path))
+    return st, path.value
 
 
 def pa_debug_stall_next(wait_limit_cycles: int) -> int:

@@ -70,10 +70,17 @@ size_t workspace_bytes(const pa_params* p, int head_dim) {
   return ws_layout(p->batch, p->num_kv_heads, max_splits_for(p->max_ctx_len), R, head_dim).total;
 }
 
-bool strides16(const pa_params* p, const void* k, const void* v) {
-  return aligned(k, 16) && aligned(v, 16) && p->k_page_stride % 16 == 0 && p->k_token_stride % 16 == 0 &&
-         p->k_head_stride % 16 == 0 && p->v_page_stride % 16 == 0 && p->v_token_stride % 16 == 0 &&
-         p->v_head_stride % 16 == 0;
+bool strides16(const pa_params* p) {
+  return p->k_page_stride % 16 == 0 && p->k_token_stride % 16 == 0 && p->k_head_stride % 16 == 0 &&
+         p->v_page_stride % 16 == 0 && p->v_token_stride % 16 == 0 && p->v_head_stride % 16 == 0;
+}
+
+// K/V load path from alignment alone (the tensor-map encoder may still refuse)
+KvLoad kv_load_for(const pa_params* p, const void* k, const void* v) {
+  if (!strides16(p)) return kKvLoadCopy;
+  if (aligned(k, 16) && aligned(v, 16)) return kKvLoadTma;
+  const uintptr_t km = reinterpret_cast<uintptr_t>(k) % 16, vm = reinterpret_cast<uintptr_t>(v) % 16;
+  return km == 8 && vm == 8 ? kKvLoadWindow : kKvLoadCopy;
 }
 
 // ---- TMA tensor maps ----------------------------------------------------------
@@ -137,6 +144,38 @@ bool encode_kv_tile_map(CUtensorMap* m, const void* base, const pa_params* p, bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Window view of K or V whose base lies 8 bytes past a 16-byte boundary (all
+// strides multiples of 16): 4-D view of 16-bit elements (row element, KV
+// head, slot, page) that starts 8 bytes before the base, so row element e
+// holds row bytes 2e - 8, 2e - 7, and a row spans row_bytes/2 + 4 elements.
+// Boxes of 136 elements (272 bytes) x 1 head x `slots` slots, no swizzle: a
+// box at element 128h lands the 8 bytes before row byte 256h, the 256 row
+// bytes from there and 8 bytes past them, each key's 272 bytes one after the
+// other.  Every byte read lies in a 16-byte granule that holds bytes of the
+// row itself (the row starts at 8 mod 16 and ends at 8 mod 16), so the copy
+// never touches memory outside the caller's rows' granules; elements past the
+// view (the last 8 bytes of the last fill) are filled with zeros, not read.
+bool encode_kv_window_map(CUtensorMap* m, const void* base, const pa_params* p, bool v, unsigned slots,
+                          int row_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const long long hs = v ? p->v_head_stride : p->k_head_stride;
+  const long long ts = v ? p->v_token_stride : p->k_token_stride;
+  const long long ps = v ? p->v_page_stride : p->k_page_stride;
+  cuuint64_t dims[4] = {(cuuint64_t)(row_bytes / 2 + 4), (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->page_size,
+                        (cuuint64_t)p->num_pages};
+  // with one KV head the head stride is never applied; any multiple of 16 serves
+  cuuint64_t strides[3] = {(cuuint64_t)(p->num_kv_heads == 1 ? row_bytes + 16 : hs), (cuuint64_t)ts, (cuuint64_t)ps};
+  cuuint32_t box[4] = {136, 1, slots < (unsigned)p->page_size ? slots : (cuuint32_t)p->page_size, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (cuuint64_t s : strides)
+    if (s == 0 || s % 16 != 0 || s >= (1ull << 40)) return false;
+  void* start = const_cast<uint8_t*>(static_cast<const uint8_t*>(base) - 8);
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, start, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D element view of Q [B][q_len][Hq][D] (16-bit elements): (d, query head,
 // verify query, request), boxes of 64 elements x G heads x q_len queries,
 // 128-byte swizzle.  One box is one 64-column atom of an item's packed Q tile,
@@ -189,6 +228,24 @@ void timing_slot(int kind, cudaEvent_t* a, cudaEvent_t* b) {
   *a = pool[2 * T.used[kind]];
   *b = pool[2 * T.used[kind] + 1];
   T.used[kind]++;
+}
+
+// Fills the K/V tensor maps of the load path the alignment allows and returns
+// that path, or kKvLoadCopy when the driver refuses an encoding.
+KvLoad encode_kv_maps(SplitArgs* a, const pa_params* p, const void* k, const void* v, int row_bytes) {
+  const KvLoad want = kv_load_for(p, k, v);
+  bool ok = want != kKvLoadCopy;
+  for (int m = 0; m < 4 && ok; ++m) {
+    const unsigned slots = 128u >> m;
+    ok = want == kKvLoadTma ? encode_kv_map(&a->k_maps[m], k, p, false, slots, row_bytes) &&
+                                  encode_kv_map(&a->v_maps[m], v, p, true, slots, row_bytes)
+                            : encode_kv_window_map(&a->k_maps[m], k, p, false, slots, row_bytes) &&
+                                  encode_kv_window_map(&a->v_maps[m], v, p, true, slots, row_bytes);
+  }
+  if (ok && want == kKvLoadTma)
+    ok = encode_kv_tile_map(&a->k_map_tile, k, p, false, row_bytes) &&
+         encode_kv_tile_map(&a->v_map_tile, v, p, true, row_bytes);
+  return ok ? want : kKvLoadCopy;
 }
 
 int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k_pages, const void* v_pages,
@@ -246,18 +303,12 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;
   a.q_len = p->q_len, a.R = R, a.page_size = p->page_size, a.mpr = p->max_pages_per_req;
   a.num_pages = p->num_pages, a.max_ctx = p->max_ctx_len, a.s_max = s_max;
-  // TMA loads need 16-byte aligned bases and strides; 8-byte aligned data uses cp.async
-  a.use_tma = strides16(p, k_pages, v_pages);
-  for (int m = 0; m < 4 && a.use_tma; ++m) {
-    const unsigned slots = 128u >> m;
-    a.use_tma = encode_kv_map(&a.k_maps[m], k_pages, p, false, slots, row_bytes) &&
-                encode_kv_map(&a.v_maps[m], v_pages, p, true, slots, row_bytes);
-  }
-  a.use_tma = a.use_tma && encode_kv_tile_map(&a.k_map_tile, k_pages, p, false, row_bytes) &&
-              encode_kv_tile_map(&a.v_map_tile, v_pages, p, true, row_bytes);
-  // the packed Q tile by TMA together with K and V; with 8-byte aligned K/V
-  // the kernel runs its per-lane copy paths for all three
-  a.q_tma = a.use_tma && encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
+  // TMA boxes for 16-byte aligned K/V, TMA windows for bases 8 bytes past a
+  // 16-byte boundary, cp.async for the rest (or where an encoding is refused)
+  a.kv_load = encode_kv_maps(&a, p, k_pages, v_pages, row_bytes);
+  // the packed Q tile by TMA together with K and V; with K/V by cp.async the
+  // kernel runs its per-lane copy paths for all three
+  a.q_tma = a.kv_load != kKvLoadCopy && encode_q_map(&a.q_map, q, p, D) ? 1 : 0;
   const long long stall = g_stall_next.exchange(0);
   a.wait_limit = stall > 0 ? stall : 0;
   a.withhold_q = stall > 0 ? 1 : 0;
@@ -436,6 +487,19 @@ int pa_debug_gather_fp8(const pa_params* p, const void* k_pages, const void* v_p
                           p->max_pages_per_req, p->num_pages, p->max_ctx_len, 256, static_cast<uint8_t*>(dst),
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+int pa_debug_kv_load_path(const pa_params* p, int32_t head_dim, int32_t elem_bytes, const void* k_pages,
+                          const void* v_pages, int32_t* path) {
+  if (!p || !k_pages || !v_pages || !path) return PA_ERR_NULL;
+  if ((head_dim != 128 && head_dim != 256) || (elem_bytes != 1 && elem_bytes != 2)) return PA_ERR_UNSUPPORTED;
+  int R = 0;
+  const int st = check_geometry(p, head_dim, &R);
+  if (st != PA_OK) return st;
+  if (!aligned(k_pages, 8) || !aligned(v_pages, 8)) return PA_ERR_ALIGN;
+  SplitArgs a;
+  *path = (int32_t)encode_kv_maps(&a, p, k_pages, v_pages, head_dim * elem_bytes);
   return PA_OK;
 }
 

@@ -12,16 +12,27 @@ namespace pa {
 // (head_dim 256).
 enum KvFormat : int { kKvE4m3 = 0, kKvBf16 = 1, kKvE5m2 = 2, kKvF16 = 3, kKvBf16D256 = 4 };
 
+// How the split kernel moves K and V rows into shared memory.
+//   kKvLoadTma:    16-byte aligned bases and strides; TMA boxes with the
+//                  128-byte swizzle, 256 row bytes per staged key.
+//   kKvLoadWindow: bases 8 bytes past a 16-byte boundary, strides multiples of
+//                  16; TMA boxes of 272-byte windows that start 8 bytes before
+//                  each 256 row bytes (no swizzle).
+//   kKvLoadCopy:   anything else 8-byte aligned; 8-byte cp.async by a warp.
+enum KvLoad : int { kKvLoadCopy = 0, kKvLoadTma = 1, kKvLoadWindow = 2 };
+
 // Split-KV kernel arguments (every element format).
 struct SplitArgs {
-  // 4-D byte views (row byte, KV head, slot, page) of K and V for the TMA
-  // loaders, with boxes of 128 bytes x 128, 64, 32 and 16 slots; filled when
-  // use_tma != 0 (16-byte aligned bases and strides)
+  // 4-D views (row, KV head, slot, page) of K and V for the TMA loaders, with
+  // boxes of 128, 64, 32 and 16 slots.  kKvLoadTma: byte elements, boxes of
+  // 128 row bytes.  kKvLoadWindow: 16-bit elements from 8 bytes before the
+  // base, boxes of 136 elements (272 bytes) of which the last 8 bytes lie
+  // past the row's end (outside the view, so filled with zeros, not read).
   CUtensorMap k_maps[4];
   CUtensorMap v_maps[4];
-  // 5-D byte views (row byte 0..127, KV head, slot, 128-byte part of the key
-  // row, page) with one box of 128 slots x 2 parts: a whole staging tile (128
-  // keys x 256 row bytes) inside one page in one copy; filled with the above
+  // kKvLoadTma only: 5-D byte views (row byte 0..127, KV head, slot, 128-byte
+  // part of the key row, page) with one box of 128 slots x 2 parts: a whole
+  // staging tile (128 keys x 256 row bytes) inside one page in one copy
   CUtensorMap k_map_tile;
   CUtensorMap v_map_tile;
   // 4-D element view of Q (d, query head, verify query, request) with boxes of
@@ -29,7 +40,7 @@ struct SplitArgs {
   // packed tile); used when q_tma != 0
   CUtensorMap q_map;
   int q_tma;
-  int use_tma;
+  int kv_load;                 // KvLoad
   const void* q;               // FP16 or BF16 (the BF16 formats) [B][q_len][Hq][D]
   const uint8_t* k;            // K base: element (page, slot, head, d) at k + page*k_ps + slot*k_ts + head*k_hs
   const uint8_t* v;

@@ -127,7 +127,9 @@ struct F16Fmt {
 
 constexpr int kChunkKeys = 32;     // one chunk = one quarter of a tile = the keys of one decode warp
 constexpr int kPageSeg = 8;       // chunks whose page ids a cp.async loader lane holds in registers
-constexpr int kStageBytes = kTileKeys * 256;  // one tile of 256-byte key rows
+constexpr int kStageBytes = kTileKeys * 256;  // one tile of 256-byte key rows (swizzled TMA and cp.async)
+constexpr int kWinRowBytes = 272;             // staged window of one key (TMA windows): 8 + 256 + 8 bytes
+constexpr int kStageAlloc = kTileKeys * kWinRowBytes;  // staging tile reserved for either layout
 constexpr float kTau = 8.0f;       // a row's reference max moves only when a score exceeds it by 2^8
 constexpr float kNoMax = -1e30f;   // reference max of a row that has seen no key (finite: 2^(s - kNoMax) never NaN)
 constexpr int kThreads = 640;
@@ -165,7 +167,7 @@ static_assert(offsetof(Misc, mref) % 16 == 0, "mref is read with 16-byte loads")
 // format and packed-row count NM:
 //   Q    K-major Q tile, D/64 atoms of NM rows x 128 B
 //   P    kPBufs P^T buffers, 128 keys x 128 B (MN-major, up to 64 rows)
-//   Kst  K staging tile, 128 keys x 256 B
+//   Kst  K staging tile, 128 keys x 256 B (swizzled) or x 272 B (windows)
 //   Vst  V staging tile, the same
 //   V    V' ring: slots of one 32-key quarter, D/64 atoms of 32 keys x 128 B,
 //        as many as fit (a quarter is released as soon as its PV MMAs finish)
@@ -178,13 +180,14 @@ struct Layout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kQBytes;
   static constexpr int kOffKst = kOffP + kPBufs * 16384;
-  static constexpr int kOffVst = kOffKst + kStageBytes;
-  static constexpr int kOffV = kOffVst + kStageBytes;
+  static constexpr int kOffVst = kOffKst + kStageAlloc;
+  static constexpr int kOffV = kOffVst + kStageAlloc;
   static constexpr int kVFit = (kSmemLimit - kOffV - (int)sizeof(Misc) - 1024) / kVQuarter;
   static constexpr int kVSlots = kVFit < kMaxVSlots ? kVFit : kMaxVSlots;
   static constexpr int kOffMisc = kOffV + kVSlots * kVQuarter;
   static constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc) + 1024;
   static_assert(kQAtom % 1024 == 0, "Q atoms must keep the 1024-byte swizzle alignment");
+  static_assert(kStageAlloc % 1024 == 0, "staging tiles must keep the 1024-byte swizzle alignment");
   static_assert(kVSlots >= 4, "the V' ring must hold a whole tile");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory map exceeds the per-block limit");
 };
@@ -292,6 +295,31 @@ __device__ __forceinline__ void load_stage_row(const uint8_t* stage, int kk, boo
                   : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// The same from a window-layout stage (kKvLoadWindow): key kk's window at
+// kk*272 holds its 256 row bytes at window bytes 8..263, so 16-byte piece p
+// is the upper half of window granule p and the lower half of granule p + 1.
+// Eight consecutive keys read granule g at (17kk + g) mod 8 of the 16-byte
+// bank groups: all different, so no bank conflicts.
+__device__ __forceinline__ void load_window_row(const uint8_t* stage, int kk, bool live, uint4 (&raw)[16]) {
+  const uint8_t* row = stage + kk * kWinRowBytes;
+  uint4 lo = live ? *reinterpret_cast<const uint4*>(row) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const uint4 hi = live ? *reinterpret_cast<const uint4*>(row + 16 * (p + 1)) : make_uint4(0u, 0u, 0u, 0u);
+    raw[p] = make_uint4(lo.z, lo.w, hi.x, hi.y);
+    lo = hi;
+  }
+}
+
+template <bool Win>
+__device__ __forceinline__ void load_row(const uint8_t* stage, int kk, bool live, uint4 (&raw)[16]) {
+  if constexpr (Win) {
+    load_window_row(stage, kk, live, raw);
+  } else {
+    load_stage_row(stage, kk, live, raw);
+  }
+}
+
 // K and V loaders: one tile (128 keys) at a time into the tensor's staging
 // tile.  Layout: two halves of the 256-byte key rows, half h at h*16384, key
 // kk's 128 bytes at kk*128 with its 16-byte piece p at ((p ^ (kk & 7)) * 16)
@@ -314,7 +342,10 @@ __device__ __forceinline__ int ld_page_id(const int32_t* p) {
 // the tile's keys are cut at page boundaries; each piece (a multiple of 16
 // slots inside one page) is covered by boxes of 128, 64, 32 and 16 slots of
 // the 4-D byte view (row byte, KV head, slot, page), two boxes (row bytes
-// 0-127 and 128-255) per piece of slots.  Completion is
+// 0-127 and 128-255) per piece of slots.  Window mode (Win, bases 8 bytes
+// past a 16-byte boundary): one box of 272-byte windows per piece of slots
+// (a whole in-page tile is one box of 128 slots), each key's window at
+// kk*272 of the stage.  Completion is
 // counted in bytes on the tile's full barrier; the thread arrives with the
 // byte total after issuing the copies.  Page ids are kept for the current
 // page index and the three after it, each loaded several pages ahead.  The
@@ -322,7 +353,7 @@ __device__ __forceinline__ int ld_page_id(const int32_t* p) {
 // queues are busy with the decode warps' traffic.  With two fills per tile
 // (512-byte rows) the pieces are walked twice, fill h copying row bytes
 // 256h .. 256h+255.
-template <class Fmt>
+template <class Fmt, bool Win>
 __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, bool is_v, uint8_t* stage) {
   const CUtensorMap* maps = is_v ? a.v_maps : a.k_maps;  // boxes of 128, 64, 32, 16 slots
   const CUtensorMap* tile_map = is_v ? &a.v_map_tile : &a.k_map_tile;  // 128 slots x both parts
@@ -374,7 +405,23 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
             pq[3] = q_cur + 3 <= q_last ? ld_page_id(bt + q_cur + 3) : -1;
           }
           const int pg = pq[0];
-          if ((unsigned)pg < (unsigned)a.num_pages && len == kTileKeys) {
+          if constexpr (Win) {
+            if ((unsigned)pg < (unsigned)a.num_pages) {
+              // window element 128h is the byte 8 before row byte 256h
+              int rr = r, sl = slot, left = len;
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int box = kTileKeys >> m;  // 128, 64, 32, 16 slots
+                while (left >= box) {
+                  tma_load_4d_hint(dst_base + rr * kWinRowBytes, maps + m, 128 * h, x.g, sl, pg, full, once);
+                  bytes += box * kWinRowBytes;
+                  rr += box, sl += box, left -= box;
+                }
+              }
+            } else {
+              bad = true;
+            }
+          } else if ((unsigned)pg < (unsigned)a.num_pages && len == kTileKeys) {
             // the whole tile inside one page: one box writes both parts
             tma_load_5d_hint(dst_base, tile_map, 0, x.g, slot, 2 * h, pg, full, once);
             bytes += kTileKeys * 256;
@@ -627,7 +674,7 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
 // K decode: warp quarter i owns TMEM lanes 32i..32i+31 = keys 32i.. of each
 // tile; lane = key, column c holds elements d = 2c, 2c+1.  With two staging
 // fills per tile, fill h supplies columns 64h .. 64h+63.
-template <class Fmt>
+template <class Fmt, bool Win>
 __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i, int lane, uint32_t tb,
                                              const uint8_t* stage) {
   WaitCtl* abort = &M.ctl;
@@ -643,7 +690,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
         // stage back at once, so the loader's refill does not wait for the
         // tensor core
         uint4 raw[16];
-        load_stage_row(stage, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
+        load_row<Win>(stage, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.kst_empty);
         // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
@@ -684,7 +731,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
 // kq*128 + ((((d%64)/8) ^ (kq%8)) * 16) + (d%8)*2.  A slot is rewritten once
 // the PV of the tile that read its previous quarter has completed; the four
 // warps signal the tile's quarters on one barrier.
-template <class Fmt, int NM>
+template <class Fmt, int NM, bool Win>
 __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i, int lane, const uint8_t* stage,
                                              uint8_t* vring) {
   using L = Layout<Fmt, NM>;
@@ -702,7 +749,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
         if (!mbar_wait(&M.vst_full, f & 1, abort)) return;
         // row into registers, stage back to the loader, then wait for the slot
         uint4 raw[16];
-        load_stage_row(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
+        load_row<Win>(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.vst_empty);
         if (h == 0 && c >= (uint32_t)L::kVSlots) {
@@ -1150,8 +1197,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    mbar_init(&M.kst_full, a.use_tma ? 1 : 32);
-    mbar_init(&M.vst_full, a.use_tma ? 1 : 32);
+    mbar_init(&M.kst_full, TMA != 0 ? 1 : 32);
+    mbar_init(&M.vst_full, TMA != 0 ? 1 : 32);
     mbar_init(&M.kst_empty, 4);
     mbar_init(&M.vst_empty, 4);
     for (int s = 0; s < 2; ++s) {
@@ -1196,11 +1243,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   if (warp == 3 || warp == 9) {
     const bool is_v = warp == 9;
     // TMA: 1 = one thread (pages of a tile or more), 2 = the warp (shorter
-    // pages); a separate instantiation each, so no kernel carries both
+    // pages), 3 = one thread, 272-byte windows (bases 8 bytes past a 16-byte
+    // boundary); a separate instantiation each, so no kernel carries two
     if constexpr (TMA == 2) {
       role_loader_tma_blocks<Fmt>(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst), lane);
-    } else if constexpr (TMA == 1) {
-      if (lane == 0) role_loader_tma<Fmt>(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst));
+    } else if constexpr (TMA == 1 || TMA == 3) {
+      if (lane == 0) role_loader_tma<Fmt, TMA == 3>(a, M, is_v, sm + (is_v ? L::kOffVst : L::kOffKst));
     } else {
       role_loader_cp<Fmt>(a, M, is_v, lane, sm + (is_v ? L::kOffVst : L::kOffKst));
     }
@@ -1225,9 +1273,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
-    role_kdecode<Fmt>(a, M, warp - 4, lane, tb, sm + L::kOffKst);
+    role_kdecode<Fmt, TMA == 3>(a, M, warp - 4, lane, tb, sm + L::kOffKst);
   } else if (vq >= 0) {
-    role_vdecode<Fmt, NM>(a, M, vq, lane, sm + L::kOffVst, sm + L::kOffV);
+    role_vdecode<Fmt, NM, TMA == 3>(a, M, vq, lane, sm + L::kOffVst, sm + L::kOffV);
   } else {
     role_softmax<Fmt, NM>(a, M, (warp - 12) / 4, warp & 3, lane, tb, sm + L::kOffP);
   }
@@ -1293,7 +1341,8 @@ cudaError_t launch_mode(const SplitArgs& a, int grid, cudaStream_t stream) {
 // own translation unit, split_kv_<format>.cu, so they compile in parallel).
 #define PA_DEFINE_SPLIT_LAUNCHER(name, Fmt)                                          \
   cudaError_t name(const SplitArgs& a, int grid, cudaStream_t stream) {              \
-    if (!a.use_tma) return launch_mode<Fmt, 0>(a, grid, stream);                     \
+    if (a.kv_load == kKvLoadCopy) return launch_mode<Fmt, 0>(a, grid, stream);       \
+    if (a.kv_load == kKvLoadWindow) return launch_mode<Fmt, 3>(a, grid, stream);     \
     return a.page_size < kTileKeys ? launch_mode<Fmt, 2>(a, grid, stream)            \
                                    : launch_mode<Fmt, 1>(a, grid, stream);           \
   }

@@ -58,7 +58,9 @@ class Spec:
     ctx_range: Optional[tuple[int, int]] = None  # uniform integer lengths in [lo, hi]
     zero_slots: Sequence[int] = ()             # live slots forced to length 0
     padded_slots: Sequence[int] = ()           # padded slots: length 0, Q = NaN
-    layout: str = "separate"       # "separate": K pages then V pages; "interleaved": [.., Hkv, 2, D]
+    layout: str = "separate"       # "separate": K pages then V pages; "interleaved": [.., Hkv, 2, D];
+                                   # "padded_tokens": separate, each slot's Hkv rows followed by 8 unused
+                                   # bytes (token strides 8 past a multiple of 16)
     base_pad: int = 0              # byte offset of the K/V base (8 gives 8-byte-only alignment)
     extra_pages: int = 0           # unused pages in the pool
 
@@ -212,6 +214,16 @@ def generate(spec: Spec, seed: int, device: str | torch.device = "cpu",
         view[:, :, :, 1, :] = vb.reshape(num_pages, ps, Hkv, row)
         strides = (ps * Hkv * 2 * row, Hkv * 2 * row, 2 * row)
         k_off, v_off = pad, pad + row
+        k_str = v_str = strides
+    elif spec.layout == "padded_tokens":
+        tstride = Hkv * row + 8
+        region = num_pages * ps * tstride
+        kv = torch.zeros(pad + 2 * region + 16, dtype=torch.uint8, device=device)
+        for off, src in ((pad, kb), (pad + region, vb)):
+            view = kv[off:off + region].view(num_pages, ps, tstride)
+            view[:, :, :Hkv * row] = src.reshape(num_pages, ps, Hkv * row)
+        strides = (ps * tstride, tstride, row)
+        k_off, v_off = pad, pad + region
         k_str = v_str = strides
     else:
         raise ValueError(spec.layout)

@@ -149,8 +149,9 @@ def _bruteforce(lib, kind, **kw):
 
 
 def pin_bruteforce_fp8(lib):
-    return _bruteforce(lib, "fp8") + _bruteforce(lib, "fp8", Hkv=1, group=6, q_len=8, layout="interleaved",
-                                                 base_pad=8)
+    return (_bruteforce(lib, "fp8") +
+            _bruteforce(lib, "fp8", Hkv=1, group=6, q_len=8, layout="interleaved", base_pad=8) +
+            _bruteforce(lib, "fp8", layout="padded_tokens", base_pad=8))
 
 
 def pin_bruteforce_e5m2(lib):

@@ -71,7 +71,40 @@ SMALL = [
     ("bf16_d256_g4_q1", "bf16", [2000, 17], dict(D=256, Hkv=2, group=4, q_len=1, page_size=64)),
     ("bf16_d128", "bf16", [1500, 2048, 17], dict(Hkv=8, group=4, q_len=1)),
     ("bf16_d128_q4_8B", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="interleaved", base_pad=8)),
+    # bases 8 bytes past a 16-byte boundary with 16-byte strides load through
+    # TMA windows: pieces of 64 + 16 slots, whole in-page tiles, many splits
+    ("fp8_page80_window", "fp8", [1000, 333], dict(Hkv=2, page_size=80, layout="interleaved", base_pad=8)),
+    ("fp8_page208_window_splits", "fp8", [20000, 4097], dict(page_size=208, layout="interleaved", base_pad=8)),
+    ("e5m2_page144_window", "e5m2", [900, 131], dict(Hkv=2, page_size=144, layout="interleaved", base_pad=8)),
+    ("f16_page208_window", "f16", [3000, 129], dict(page_size=208, layout="interleaved", base_pad=8)),
+    ("bf16_d256_page144_window", "bf16", [1500, 77],
+     dict(D=256, Hkv=2, page_size=144, layout="interleaved", base_pad=8)),
+    # token strides 8 past a multiple of 16: the cp.async loader
+    ("fp8_padded_tokens_copy", "fp8", [700, 129, 0], dict(Hkv=2, page_size=32, layout="padded_tokens", base_pad=8)),
+    ("e5m2_padded_tokens_copy", "e5m2", [300, 37], dict(layout="padded_tokens")),
+    ("f16_padded_tokens_copy", "f16", [700, 129, 0], dict(Hkv=2, page_size=32, layout="padded_tokens")),
+    ("bf16_d256_padded_tokens_copy", "bf16", [500, 33], dict(D=256, Hkv=2, layout="padded_tokens")),
+    ("bf16_d128_padded_tokens_copy", "bf16", [333, 1], dict(Hkv=2, group=4, q_len=4, layout="padded_tokens")),
 ]
+
+
+def _expected_load_path(kw):
+    if kw.get("layout") == "padded_tokens":
+        return B.PA_KV_LOAD_COPY
+    return B.PA_KV_LOAD_WINDOW if kw.get("base_pad", 0) == 8 else B.PA_KV_LOAD_TMA
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_load_path_of_each_layout(case):
+    """Each parity case runs the K/V load path its alignment calls for: the
+    CUDA driver accepts every tensor map, so nothing falls back silently."""
+    _, kind, lens, kw = case
+    w = _small(kind, lens, **kw)
+    kv = w.kv.data_ptr()
+    st, path = B.pa_debug_kv_load_path(D.params_for(w), w.spec.head_dim, w.spec.elem_bytes, kv + w.k_offset,
+                                       kv + w.v_offset)
+    assert st == B.PA_OK
+    assert path == _expected_load_path(kw)
 
 
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
@@ -217,6 +250,10 @@ def test_config_b8_l128k_16bit_sampled(name):
 
 def test_config_b16_mixed_sampled():
     w = _full("b16_mixed")
+    kv = w.kv.data_ptr()
+    # 8-byte-only aligned bases with 16-byte strides: TMA windows
+    assert B.pa_debug_kv_load_path(D.params_for(w), 256, 1, kv + w.k_offset, kv + w.v_offset) == \
+        (B.PA_OK, B.PA_KV_LOAD_WINDOW)
     dec = D.Decoder(w)
     dec.run()
     torch.cuda.synchronize()
