@@ -266,6 +266,65 @@ int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, 
                         const int32_t* block_table, const int32_t* ctx_lens, void* out, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- causal prefill, FP16 Q/K/V, head_dim 256 ---------------------------------
+ *
+ * The long-prefill phase of the same attention ("SM70 attention and quantized
+ * projection coverage across TP sizes", sections "Scope" and "Accumulation
+ * audit and rejected tuning": Q8192 x KV262144 causal prefill for GQA-6,
+ * head_dim 256, FP16 inputs and intermediates, FP32 accumulation of both QK
+ * and PV).  For request b, query i < q_len and query head h (KV head
+ * h / (num_q_heads / num_kv_heads)), the q_len queries are the last q_len
+ * positions of a context of kv_len keys, so query i sees keys
+ * 0 .. kv_len - q_len + i:
+ *   out[b][i][h] = sum_j exp(s_j - max s) v_j / sum_j exp(s_j - max s),
+ *   s_j = q . k_j / 16,  lse[b][i][h] = max s + log(sum_j exp(s_j - max s)).
+ * A query that sees no key (kv_len < q_len, i < q_len - kv_len) gets zeros
+ * and lse = -inf.  The keys are cut into splits whose length depends on
+ * kv_len alone (pa_prefill_plan); each (128-query tile, split) is computed
+ * with P = exp(s - m) rounded to FP16 before the PV product, and the splits
+ * are merged in ascending order, so every output row's bits are independent
+ * of batch and of num_q_heads / num_kv_heads. */
+typedef struct pa_prefill_params {
+  int32_t batch;        /* requests, 1 .. 64 */
+  int32_t q_len;        /* queries per request, 1 .. 65536 */
+  int32_t kv_len;       /* keys per request, 1 .. 4194304 */
+  int32_t num_q_heads;  /* Hq, a multiple of num_kv_heads, at most 256 */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t head_dim;     /* 256 */
+  /* element strides of K and V: element (b, key t, kv head g, d) of K is at
+   * k + b*k_batch_stride + t*k_token_stride + g*k_head_stride + d (FP16
+   * elements); V likewise.  Every stride a positive multiple of 8 elements
+   * (16 bytes) or, for an extent of 1 (batch 1, one KV head), any value. */
+  int64_t k_batch_stride, k_token_stride, k_head_stride;
+  int64_t v_batch_stride, v_token_stride, v_head_stride;
+} pa_prefill_params;
+
+/* Key split of the prefill for kv_len keys: *num_splits splits of *split_len
+ * keys (the last one shorter): split_len = 32768 above 32768 keys, else
+ * kv_len / 8 rounded up to a multiple of 128 and at least 1024.  Returns
+ * PA_ERR_NULL or PA_ERR_SHAPE (kv_len < 1). */
+int pa_prefill_plan(int32_t kv_len, int32_t* num_splits, int32_t* split_len);
+
+/* Workspace bytes a pa_prefill_f16 call with this geometry needs (0 when the
+ * geometry is invalid): the status word and the FP32 split partials. */
+size_t pa_prefill_f16_workspace_bytes(const pa_prefill_params* p);
+
+/* q         FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned.
+ * k, v      FP16, addressed through the strides in *p, 16-byte aligned.
+ * out       FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned; fully written.
+ * lse       nullable FP32 [batch][q_len][num_q_heads] (natural log).
+ * workspace device buffer of at least pa_prefill_f16_workspace_bytes(p) bytes,
+ *           256-byte aligned, status word zero; two calls in flight at the
+ *           same time must use different workspaces.
+ * stream    cudaStream_t (NULL = legacy default stream).
+ * Two kernels run on the stream: the tcgen05 attention kernel over (tile,
+ * split) work items, then the merge of the split partials.  A pipeline wait
+ * that exceeds its bound sets PA_FLAG_TIMEOUT in the workspace's status word
+ * (pa_read_status).  Returns PA_OK after enqueueing, or a negative pa_status
+ * (PA_ERR_UNSUPPORTED for head_dim != 256). */
+int pa_prefill_f16(const pa_prefill_params* p, const void* q, const void* k, const void* v, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- workspace bank ---------------------------------------------------------
  *
  * A host object that hands out decode workspaces ("panels") so that CUDA
@@ -370,14 +429,15 @@ int pa_debug_kv_load_path(const pa_params* p, int32_t head_dim, int32_t elem_byt
 int pa_debug_stall_next(int64_t wait_limit_cycles);
 
 /* ---- kernel timing ------------------------------------------------------------
- * pa_timing_enable(1) makes every later decode call record CUDA events around
- * its kernel (on the call's stream; one kernel per call: split-KV attention
- * followed by the log-sum-exp merge of the split partials).
+ * pa_timing_enable(1) makes every later decode or prefill call record CUDA
+ * events around its attention kernel (on the call's stream; a decode call is
+ * one kernel: split-KV attention followed by the log-sum-exp merge of the
+ * split partials).
  * pa_timing_collect synchronises those events and returns, for kernel 0 (the
- * decode kernel), the summed device time in milliseconds and the number of
- * launches timed since the previous collect, then resets them; kernel 1 is
- * kept for compatibility and reports no launches.  Recording stops while
- * disabled.  At most 4096 launches are kept. */
+ * decode kernel) or kernel 1 (the attention kernel of pa_prefill_f16, without
+ * its merge), the summed device time in milliseconds and the number of
+ * launches timed since the previous collect, then resets them.  Recording
+ * stops while disabled.  At most 4096 launches per kernel are kept. */
 int pa_timing_enable(int on);
 int pa_timing_collect(int kernel, double* total_ms, int64_t* launches);
 

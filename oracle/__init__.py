@@ -168,3 +168,45 @@ def paged_attn(kind: str, *, q: np.ndarray, kv: np.ndarray, k_offset: int, v_off
     if rc != 0:
         raise RuntimeError(f"oracle failed with status {rc}")
     return out, lse
+
+
+def prefill_attn(*, q: np.ndarray, k: np.ndarray, v: np.ndarray, k_strides: tuple[int, int, int],
+                 v_strides: tuple[int, int, int], kv_len: int, num_kv_heads: int, rows=None, num_threads: int = 0,
+                 lib=None):
+    """The causal long prefill ("SM70 attention and quantized projection
+    coverage across TP sizes", sections "Scope" and "Accumulation audit and
+    rejected tuning": Q8192 x KV262144, FP16 inputs) is the same definition
+    with q_len prefill queries that are the last q_len positions of a
+    kv_len-key context: query i sees keys 0 .. kv_len - q_len + i.  A request's
+    dense K and V are one page of kv_len slots, page b for request b.
+
+    q        uint16 FP16 bits [B, q_len, Hq, D].
+    k, v     uint16 FP16 bits, flat buffers; element (b, key t, kv head g, d)
+             of K at k[b*k_strides[0] + t*k_strides[1] + g*k_strides[2] + d]
+             (element strides), V likewise.
+    rows     None for all rows, else flat row ids (b*q_len + i)*Hq + h.
+    Returns (out float64, lse float64) as ``paged_attn``.
+    """
+    lib = lib or load()
+    q = np.ascontiguousarray(q).view(np.uint16)
+    B, q_len, Hq, D = q.shape
+    k = np.ascontiguousarray(k).view(np.uint16)
+    v = np.ascontiguousarray(v).view(np.uint16)
+    bt = np.arange(B, dtype=np.int32).reshape(B, 1)
+    cl = np.full(B, int(kv_len), dtype=np.int32)
+    if rows is None:
+        out = np.empty((B, q_len, Hq, D), np.float64)
+        lse = np.empty((B, q_len, Hq), np.float64)
+        rows_arr, n_rows, rows_ptr = None, 0, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32)
+        n_rows = int(rows_arr.size)
+        out = np.empty((n_rows, D), np.float64)
+        lse = np.empty((n_rows,), np.float64)
+        rows_ptr = _ptr(rows_arr)
+    rc = lib.oracle_paged_attn_f16(B, q_len, Hq, num_kv_heads, D, int(kv_len), 1, _ptr(q), _ptr(k), _ptr(v),
+                                   *[2 * int(s) for s in k_strides], *[2 * int(s) for s in v_strides], _ptr(bt),
+                                   _ptr(cl), rows_ptr, n_rows, _ptr(out), _ptr(lse), int(num_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with status {rc}")
+    return out, lse

@@ -41,6 +41,14 @@ class pa_params(ctypes.Structure):
                 ("v_token_stride", ctypes.c_int64), ("v_head_stride", ctypes.c_int64)]
 
 
+class pa_prefill_params(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("kv_len", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("k_batch_stride", ctypes.c_int64), ("k_token_stride", ctypes.c_int64),
+                ("k_head_stride", ctypes.c_int64), ("v_batch_stride", ctypes.c_int64),
+                ("v_token_stride", ctypes.c_int64), ("v_head_stride", ctypes.c_int64)]
+
+
 _LIB = None
 _P = ctypes.POINTER
 
@@ -76,6 +84,9 @@ def load() -> ctypes.CDLL:
             "pa_decode_bf16_d128": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_bf16_d256": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_decode_f16": ([pp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "pa_prefill_plan": ([i32, _P(i32), _P(i32)], ctypes.c_int),
+            "pa_prefill_f16_workspace_bytes": ([_P(pa_prefill_params)], sz),
+            "pa_prefill_f16": ([_P(pa_prefill_params), vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "pa_bank_create": ([BANK_ALLOC_FN, BANK_FREE_FN, vp], vp),
             "pa_bank_destroy": ([vp], ctypes.c_int),
             "pa_bank_workspace": ([vp, pp, i32, vp, _P(vp), _P(sz)], ctypes.c_int),
@@ -154,6 +165,22 @@ def pa_split_plan(ctx_len: int, num_kv_heads: int = 1) -> tuple[int, int, int]:
     s, c = ctypes.c_int32(), ctypes.c_int32()
     st = load().pa_split_plan(int(ctx_len), int(num_kv_heads), ctypes.byref(s), ctypes.byref(c))
     return st, s.value, c.value
+
+
+def pa_prefill_plan(kv_len: int) -> tuple[int, int, int]:
+    """(status, num_splits, split_len) of the prefill key split."""
+    s, c = ctypes.c_int32(), ctypes.c_int32()
+    st = load().pa_prefill_plan(int(kv_len), ctypes.byref(s), ctypes.byref(c))
+    return st, s.value, c.value
+
+
+def pa_prefill_f16_workspace_bytes(p: pa_prefill_params) -> int:
+    return int(load().pa_prefill_f16_workspace_bytes(ctypes.byref(p)))
+
+
+def pa_prefill_f16(p: pa_prefill_params, q, k, v, out, lse, workspace, workspace_bytes: int, stream=None) -> int:
+    return load().pa_prefill_f16(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
 
 
 def pa_decode_fp8_workspace_bytes(p: pa_params) -> int:

@@ -328,6 +328,153 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   return PA_OK;
 }
 
+// ---- causal prefill -------------------------------------------------------------
+constexpr int kPfMaxBatch = 64;
+constexpr int kPfMaxQLen = 65536;
+constexpr int kPfMaxKv = 1 << 22;
+constexpr int kPfMaxHeads = 256;
+constexpr int kPfTile = 128;
+
+// split_len depends on kv_len alone: 32768 above 32768 keys, else kv_len / 8
+// rounded up to whole 128-key tiles, at least 1024
+void prefill_plan(int kv_len, int* num_splits, int* split_len) {
+  int len = 32768;
+  if (kv_len <= 32768) {
+    len = ((kv_len + 7) / 8 + kPfTile - 1) / kPfTile * kPfTile;
+    if (len < 1024) len = 1024;
+  }
+  *split_len = len;
+  *num_splits = (kv_len + len - 1) / len;
+}
+
+struct PfLayout {
+  size_t ml_off, o_off, total;
+  long long tiles;  // (request, head, query tile, split) partial tiles
+};
+
+int check_prefill(const pa_prefill_params* p) {
+  if (p == nullptr) return PA_ERR_NULL;
+  if (p->head_dim != 256) return PA_ERR_UNSUPPORTED;
+  if (p->batch < 1 || p->batch > kPfMaxBatch || p->q_len < 1 || p->q_len > kPfMaxQLen || p->kv_len < 1 ||
+      p->kv_len > kPfMaxKv)
+    return PA_ERR_SHAPE;
+  if (p->num_kv_heads < 1 || p->num_q_heads < 1 || p->num_q_heads > kPfMaxHeads ||
+      p->num_q_heads % p->num_kv_heads != 0)
+    return PA_ERR_SHAPE;
+  const long long st[6] = {p->k_batch_stride, p->k_token_stride, p->k_head_stride,
+                           p->v_batch_stride, p->v_token_stride, p->v_head_stride};
+  const bool unit[6] = {p->batch == 1, false, p->num_kv_heads == 1, p->batch == 1, false, p->num_kv_heads == 1};
+  for (int i = 0; i < 6; ++i) {
+    if (unit[i]) continue;
+    if (st[i] <= 0) return PA_ERR_SHAPE;
+    if (st[i] % 8 != 0) return PA_ERR_ALIGN;
+  }
+  return PA_OK;
+}
+
+PfLayout prefill_layout(const pa_prefill_params* p) {
+  int ns = 0, len = 0;
+  prefill_plan(p->kv_len, &ns, &len);
+  const long long n_qt = (p->q_len + kPfTile - 1) / kPfTile;
+  PfLayout L;
+  L.tiles = (long long)p->batch * p->num_q_heads * n_qt * ns;
+  const size_t rows = (size_t)L.tiles * kPfTile;
+  L.ml_off = 256;
+  L.o_off = L.ml_off + (rows * sizeof(float2) + 255) / 256 * 256;
+  L.total = L.o_off + rows * 256 * sizeof(float);
+  return L;
+}
+
+// byte stride of a dimension; one of extent 1 is never applied, so any
+// multiple of 16 serves
+cuuint64_t pf_stride(long long elems, bool unit) { return unit ? 1024 : (cuuint64_t)elems * 2; }
+
+bool encode_prefill_maps(PrefillArgs* a, const pa_prefill_params* p, const void* q, const void* k, const void* v) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const auto il = CU_TENSOR_MAP_INTERLEAVE_NONE;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  const auto oob = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE;
+  const bool b1 = p->batch == 1, h1 = p->num_kv_heads == 1;
+  // Q: (d within atom, query, atom, head, request)
+  {
+    const cuuint64_t row = (cuuint64_t)p->num_q_heads * 512;
+    cuuint64_t dims[5] = {64, (cuuint64_t)p->q_len, 4, (cuuint64_t)p->num_q_heads, (cuuint64_t)p->batch};
+    cuuint64_t strides[4] = {row, 128, 512, b1 ? 1024 : row * (cuuint64_t)p->q_len};
+    cuuint32_t box[5] = {64, 128, 4, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (enc(&a->q_map, f16, 5, const_cast<void*>(q), dims, strides, box, estr, il, sw, l2, oob) != CUDA_SUCCESS)
+      return false;
+  }
+  // K: (d, KV head, key, request)
+  {
+    cuuint64_t dims[4] = {256, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->kv_len, (cuuint64_t)p->batch};
+    cuuint64_t strides[3] = {pf_stride(p->k_head_stride, h1), pf_stride(p->k_token_stride, false),
+                             pf_stride(p->k_batch_stride, b1)};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(&a->k_map, f16, 4, const_cast<void*>(k), dims, strides, box, estr, il, sw, l2, oob) != CUDA_SUCCESS)
+      return false;
+  }
+  // V: (d within atom, key, atom, KV head, request)
+  {
+    cuuint64_t dims[5] = {64, (cuuint64_t)p->kv_len, 4, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->batch};
+    cuuint64_t strides[4] = {pf_stride(p->v_token_stride, false), 128, pf_stride(p->v_head_stride, h1),
+                             pf_stride(p->v_batch_stride, b1)};
+    cuuint32_t box[5] = {64, 32, 4, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (enc(&a->v_map, f16, 5, const_cast<void*>(v), dims, strides, box, estr, il, sw, l2, oob) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+int prefill_f16(const pa_prefill_params* p, const void* q, const void* k, const void* v, void* out, float* lse,
+                void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  int st = check_prefill(p);
+  if (st != PA_OK) return st;
+  if (!q || !k || !v || !out) return PA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return PA_ERR_ALIGN;
+  const PfLayout L = prefill_layout(p);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return PA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  const int nsm = sm_count(dev);
+  if (nsm <= 0) return PA_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_prefill_maps(&a, p, q, k, v)) return PA_ERR_CUDA;
+  a.part_ml = reinterpret_cast<float2*>(ws + L.ml_off);
+  a.part_o = reinterpret_cast<float*>(ws + L.o_off);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.B = p->batch, a.q_len = p->q_len, a.kv_len = p->kv_len, a.Hq = p->num_q_heads, a.Hkv = p->num_kv_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.n_qt = (p->q_len + kPfTile - 1) / kPfTile;
+  prefill_plan(p->kv_len, &a.num_splits, &a.split_len);
+  if (L.tiles > 0x7fffffffll) return PA_ERR_SHAPE;
+  a.total_items = (int)L.tiles;
+  a.wait_limit = 0;
+  const int grid = a.total_items < nsm ? a.total_items : nsm;
+
+  cudaEvent_t e0, e1;
+  timing_slot(1, &e0, &e1);
+  if (e0) cudaEventRecord(e0, stream);
+  if (launch_prefill(a, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (e1) cudaEventRecord(e1, stream);
+  PrefillMergeArgs m;
+  m.part_o = a.part_o, m.part_ml = a.part_ml, m.out = out, m.lse = lse;
+  m.B = a.B, m.q_len = a.q_len, m.kv_len = a.kv_len, m.Hq = a.Hq, m.n_qt = a.n_qt, m.split_len = a.split_len;
+  m.num_splits = a.num_splits;
+  if (launch_prefill_merge(m, stream) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 // ---- allocation-free variant ------------------------------------------------
 // Scratch for pa_decode_fp8_noalloc: a module-scope device array that every
 // device loading this library holds until the process exits.  Host code must
@@ -440,6 +587,26 @@ int pa_decode_bf16_d128(const pa_params* p, const void* q, const void* k_pages, 
                         size_t workspace_bytes_given, void* stream) {
   return decode_common(kKvBf16, p, q, k_pages, v_pages, block_table, ctx_lens, nullptr, nullptr, out, lse, workspace,
                        workspace_bytes_given, stream);
+}
+
+int pa_prefill_plan(int32_t kv_len, int32_t* num_splits, int32_t* split_len) {
+  if (!num_splits || !split_len) return PA_ERR_NULL;
+  if (kv_len < 1) return PA_ERR_SHAPE;
+  int ns = 0, len = 0;
+  prefill_plan(kv_len, &ns, &len);
+  *num_splits = ns;
+  *split_len = len;
+  return PA_OK;
+}
+
+size_t pa_prefill_f16_workspace_bytes(const pa_prefill_params* p) {
+  if (check_prefill(p) != PA_OK) return 0;
+  return prefill_layout(p).total;
+}
+
+int pa_prefill_f16(const pa_prefill_params* p, const void* q, const void* k, const void* v, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return prefill_f16(p, q, k, v, out, lse, workspace, workspace_bytes, stream);
 }
 
 int pa_read_status(const void* workspace, uint32_t* flags, void* stream) {

@@ -63,6 +63,38 @@ struct SplitArgs {
 };
 
 
+// Causal prefill kernel arguments (FP16 Q/K/V, head_dim 256).  Work item
+// it = ((s * B + b) * n_qt + qt) * Hq + h: query tile qt (128 queries) of
+// query head h of request b against key split s (split_len keys).
+struct PrefillArgs {
+  // Q [B][q_len][Hq][256]: 5-D view (d within a 64-column atom, query, atom,
+  // head, request), one box of 64 x 128 queries x 4 atoms = the whole tile
+  CUtensorMap q_map;
+  // K: 4-D view (d, KV head, key, request), boxes of 64 d x 128 keys
+  CUtensorMap k_map;
+  // V: 5-D view (d within atom, key, atom, KV head, request), boxes of
+  // 64 d x 32 keys x 4 atoms
+  CUtensorMap v_map;
+  float* part_o;    // FP32 partial O per (item tile, row, d), unnormalised
+  float2* part_ml;  // (m in log2 units, l) per (item tile, row)
+  uint32_t* status;
+  int B, q_len, kv_len, Hq, Hkv, G, n_qt, split_len, num_splits, total_items;
+  long long wait_limit;  // pipeline wait bound in cycles (0: default)
+};
+
+// Merge of the prefill split partials into FP16 output rows and the LSE.
+struct PrefillMergeArgs {
+  const float* part_o;
+  const float2* part_ml;
+  void* out;   // FP16 [B][q_len][Hq][256]
+  float* lse;  // nullable, [B][q_len][Hq]
+  int B, q_len, kv_len, Hq, n_qt, split_len, num_splits;
+};
+
+int prefill_smem_bytes();
+cudaError_t launch_prefill(const PrefillArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_prefill_merge(const PrefillMergeArgs& m, cudaStream_t stream);
+
 int split_smem_bytes();
 cudaError_t launch_split(const SplitArgs& a, KvFormat fmt, int grid, cudaStream_t stream);
 // per-format launchers behind launch_split (split_kv_<format>.cu)

@@ -111,6 +111,15 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* map, 
 }
 
 // 5-D tiled tensor load with an L2 cache policy, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void* map, int c0, int c1, int c2, int c3, int c4,
                                                  uint64_t* bar, uint64_t policy) {
   asm volatile(

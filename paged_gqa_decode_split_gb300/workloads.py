@@ -239,3 +239,71 @@ def small_spec(kind: str = "fp8", *, batch: int = 2, num_kv_heads: int = 1, grou
     D = head_dim or (128 if kind == "bf16" else 256)
     return Spec(name, kind, batch, num_kv_heads, num_kv_heads * group, D, q_len, page_size, max_ctx_len,
                 ctx_lens=(0,) * batch, layout=layout, base_pad=base_pad)
+
+
+# ------------------------------------------------------------------ prefill --
+# Causal long prefill ("SM70 attention and quantized projection coverage
+# across TP sizes", sections "Accumulation audit and rejected tuning" and
+# "Graph replay and long-prefill follow-up": Q8192 x KV262144, GQA 6 with
+# Hkv 1/2/4, B1/B2, FP16 inputs, random values).  Q, K and V ~ N(0, 1) drawn
+# in FP32 and rounded to FP16.  K and V are dense per request
+# ([B][kv_len][Hkv][256], or with `token_pad` unused elements after each
+# token's Hkv rows to exercise the strides).
+
+@dataclasses.dataclass(frozen=True)
+class PrefillSpec:
+    name: str
+    batch: int
+    q_len: int
+    kv_len: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int = 256
+    token_pad: int = 0  # extra FP16 elements after each token's Hkv rows (a multiple of 8)
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    spec: PrefillSpec
+    q: torch.Tensor        # FP16 [B][q_len][Hq][D]
+    k_buf: torch.Tensor    # FP16 storage of K
+    v_buf: torch.Tensor
+    k_strides: tuple[int, int, int]  # (batch, token, head) in elements
+    v_strides: tuple[int, int, int]
+
+    def key_view(self, which: str) -> torch.Tensor:
+        """[B][kv_len][Hkv][D] strided view of K or V."""
+        s = self.spec
+        buf, st = (self.k_buf, self.k_strides) if which == "k" else (self.v_buf, self.v_strides)
+        return buf.as_strided((s.batch, s.kv_len, s.num_kv_heads, s.head_dim), (*st, 1))
+
+
+PREFILL_SPECS = {
+    # the pages' single-GPU prefill operator at the TP4 local geometry (Hkv 1)
+    "prefill_q8192_kv262144": PrefillSpec("prefill_q8192_kv262144", 1, 8192, 262144, 6, 1),
+    # the TP2 / TP1 local geometries, B2 (the bitwise per-head check's shapes)
+    "prefill_q8192_kv262144_hkv2_b2": PrefillSpec("prefill_q8192_kv262144_hkv2_b2", 2, 8192, 262144, 12, 2),
+}
+PREFILL_SEED = {"prefill_q8192_kv262144": 2001, "prefill_q8192_kv262144_hkv2_b2": 2002}
+
+
+def generate_prefill(spec: PrefillSpec, seed: int, device: str | torch.device = "cpu") -> PrefillWorkload:
+    """Draw one seeded prefill workload of shape ``spec`` on ``device``."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(seed)
+    B, Q, KV, Hq, Hkv, D = spec.batch, spec.q_len, spec.kv_len, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    if Hq % Hkv:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    if spec.token_pad % 8:
+        raise ValueError("token_pad must be a multiple of 8 elements")
+    q = torch.randn((B, Q, Hq, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+    tstride = Hkv * D + spec.token_pad
+    strides = (KV * tstride, tstride, D)
+    bufs = []
+    for _ in range(2):
+        x = torch.randn((B, KV, Hkv, D), generator=gen, device=device, dtype=torch.float32).to(torch.float16)
+        buf = torch.zeros(B * KV * tstride, dtype=torch.float16, device=device)
+        buf.as_strided((B, KV, Hkv, D), (*strides, 1)).copy_(x)
+        del x
+        bufs.append(buf)
+    return PrefillWorkload(spec=spec, q=q, k_buf=bufs[0], v_buf=bufs[1], k_strides=strides, v_strides=strides)

@@ -21,7 +21,10 @@ What pins what:
                         exactly which keys each verify query sees;
   * row selection     - any list of rows (shuffled, repeated) on any number of
                         threads equals, bit for bit, the same rows of a
-                        one-thread evaluation of all rows.
+                        one-thread evaluation of all rows;
+  * prefill entry     - brute force on tiny causal prefills (strided K/V, a
+                        context shorter than the query window, q_len ==
+                        kv_len) against the same SDPA routine.
 """
 from __future__ import annotations
 
@@ -330,7 +333,62 @@ def pin_row_selection_and_threads(lib):
     return fails
 
 
+def prefill_dense_reference(w: wl.PrefillWorkload):
+    """float64 SDPA over the strided K/V views of a prefill workload with an
+    explicit causal mask (query i sees keys 0 .. kv_len - q_len + i); rows
+    without a key come back as zeros / -inf."""
+    s = w.spec
+    B, Q, KV, Hq, Hkv, D = s.batch, s.q_len, s.kv_len, s.num_q_heads, s.num_kv_heads, s.head_dim
+    G = Hq // Hkv
+    q = w.q.detach().cpu().double()
+    K, V = w.key_view("k").detach().cpu().double(), w.key_view("v").detach().cpu().double()
+    mask = torch.arange(KV)[None, :] <= (KV - Q + torch.arange(Q))[:, None]
+    out = np.zeros((B, Q, Hq, D))
+    lse = np.full((B, Q, Hq), -np.inf)
+    seen = mask.any(dim=1)
+    for b in range(B):
+        for h in range(Hq):
+            kg, vg = K[b, :, h // G], V[b, :, h // G]
+            qs = q[b, :, h]
+            o = torch.nn.functional.scaled_dot_product_attention(qs[None, None], kg[None, None], vg[None, None],
+                                                                 attn_mask=mask[None, None])[0, 0]
+            sc = ((qs @ kg.T) / math.sqrt(D)).masked_fill(~mask, float("-inf"))
+            ls = torch.logsumexp(sc, dim=-1)
+            out[b, seen, h] = o[seen].numpy()
+            lse[b, seen, h] = ls[seen].numpy()
+    return out, lse
+
+
+def run_prefill_oracle(w: wl.PrefillWorkload, rows=None, lib=None, num_threads: int = 0):
+    s = w.spec
+
+    def bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    return oracle.prefill_attn(q=bits(w.q), k=bits(w.k_buf), v=bits(w.v_buf), k_strides=w.k_strides,
+                               v_strides=w.v_strides, kv_len=s.kv_len, num_kv_heads=s.num_kv_heads, rows=rows,
+                               num_threads=num_threads, lib=lib)
+
+
+def pin_prefill_bruteforce(lib):
+    """The prefill entry (dense per-request K/V as one page, q_len prefill
+    queries) against SDPA on tiny shapes: strided K/V with padded tokens, a
+    context shorter than the query window (rows without keys), and q_len ==
+    kv_len (plain causal attention)."""
+    fails = []
+    cases = [(wl.PrefillSpec("pin_a", 2, 37, 300, 6, 2, token_pad=8), 31),
+             (wl.PrefillSpec("pin_b", 1, 50, 20, 3, 1), 32),
+             (wl.PrefillSpec("pin_c", 1, 64, 64, 4, 2), 33)]
+    for spec, seed in cases:
+        w = wl.generate_prefill(spec, seed)
+        got, glse = run_prefill_oracle(w, lib=lib, num_threads=1)
+        ref, rlse = prefill_dense_reference(w)
+        fails += _cmp(f"prefill {spec.name} out", got, ref, atol=1e-12, rtol=1e-12)
+        fails += _cmp(f"prefill {spec.name} lse", glse, rlse, atol=1e-12, rtol=1e-12)
+    return fails
+
+
 ALL_PINS = [pin_e4m3_vs_torch, pin_e4m3_closed_form, pin_e4m3_golden, pin_e5m2_vs_torch, pin_e5m2_closed_form,
             pin_e5m2_golden, pin_f16_vs_numpy, pin_bf16_vs_torch,
             pin_bruteforce_fp8, pin_bruteforce_e5m2, pin_bruteforce_bf16, pin_bruteforce_f16, pin_uniform_mean, pin_single_key, pin_permutation,
-            pin_zero_length, pin_two_key, pin_causal_window, pin_row_selection_and_threads]
+            pin_zero_length, pin_two_key, pin_causal_window, pin_row_selection_and_threads, pin_prefill_bruteforce]

@@ -243,3 +243,84 @@ def test_timing_and_status_arguments(lib):
     assert st == 0 and n == 0 and ms == 0.0
     assert lib.pa_read_status(None, None, None) == B.PA_ERR_NULL
     assert lib.pa_clear_status(None, None) == B.PA_ERR_NULL
+
+
+# ------------------------------------------------------------------ prefill --
+
+def _prefill_params(**over):
+    p = B.pa_prefill_params()
+    p.batch, p.q_len, p.kv_len, p.num_q_heads, p.num_kv_heads, p.head_dim = 2, 300, 5000, 12, 2, 256
+    ts = 2 * 256 + 8
+    p.k_batch_stride, p.k_token_stride, p.k_head_stride = 5000 * ts, ts, 256
+    p.v_batch_stride, p.v_token_stride, p.v_head_stride = 5000 * ts, ts, 256
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+def _prefill_plan_restated(kv):
+    """split_len 32768 above 32768 keys, else ceil(kv / 8) rounded up to 128, at least 1024."""
+    ln = 32768 if kv > 32768 else max(1024, -(-(-(-kv // 8)) // 128) * 128)
+    return -(-kv // ln), ln
+
+
+@pytest.mark.parametrize("kv", [1, 100, 1024, 1025, 8192, 8193, 20000, 32768, 32769, 70000, 262144, 1 << 22])
+def test_prefill_plan_matches_statement(lib, kv):
+    st, ns, ln = B.pa_prefill_plan(kv)
+    assert st == B.PA_OK and (ns, ln) == _prefill_plan_restated(kv)
+    assert ln % 128 == 0 and (ns - 1) * ln < kv <= ns * ln
+
+
+def test_prefill_plan_known_values(lib):
+    assert B.pa_prefill_plan(262144)[1:] == (8, 32768)
+    assert B.pa_prefill_plan(5000)[1:] == (5, 1024)
+    assert B.pa_prefill_plan(0)[0] == B.PA_ERR_SHAPE
+    assert lib.pa_prefill_plan(10, None, None) == B.PA_ERR_NULL
+
+
+def test_prefill_workspace_size_formula(lib):
+    p = _prefill_params()
+    ns, _ = _prefill_plan_restated(p.kv_len)
+    tiles = p.batch * p.num_q_heads * math.ceil(p.q_len / 128) * ns
+    rows = tiles * 128
+    ml = (rows * 8 + 255) // 256 * 256
+    assert B.pa_prefill_f16_workspace_bytes(p) == 256 + ml + rows * 256 * 4
+    # the headline shape: 8 splits x 64 query tiles x 6 heads
+    big = _prefill_params(batch=1, q_len=8192, kv_len=262144, num_q_heads=6, num_kv_heads=1)
+    assert B.pa_prefill_f16_workspace_bytes(big) == 256 + 384 * 8 * 128 * 8 + 384 * 8 * 128 * 1024
+
+
+@pytest.mark.parametrize("over", [dict(head_dim=128), dict(batch=0), dict(batch=65), dict(q_len=0),
+                                  dict(kv_len=0), dict(num_kv_heads=5), dict(num_q_heads=0),
+                                  dict(k_token_stride=516), dict(v_head_stride=-256), dict(k_batch_stride=0)])
+def test_prefill_rejects_bad_geometry(lib, over):
+    p = _prefill_params(**over)
+    assert B.pa_prefill_f16_workspace_bytes(p) == 0
+    st = B.pa_prefill_f16(p, 256, 512, 768, 1024, None, 4096, 1 << 30, stream=0)
+    assert st in (B.PA_ERR_SHAPE, B.PA_ERR_UNSUPPORTED, B.PA_ERR_ALIGN)
+    if "head_dim" in over:
+        assert st == B.PA_ERR_UNSUPPORTED
+    if "k_token_stride" in over:
+        assert st == B.PA_ERR_ALIGN
+
+
+def test_prefill_unit_extents_take_any_stride(lib):
+    # batch 1 and one KV head: those strides are never applied
+    p = _prefill_params(batch=1, num_kv_heads=1, num_q_heads=6, k_batch_stride=0, v_batch_stride=3,
+                        k_head_stride=-1, v_head_stride=0)
+    assert B.pa_prefill_f16_workspace_bytes(p) > 0
+
+
+def test_prefill_rejects_bad_pointers_and_workspace(lib):
+    p = _prefill_params()
+    ws = B.pa_prefill_f16_workspace_bytes(p)
+    assert lib.pa_prefill_f16(None, 256, 512, 768, 1024, None, 4096, ws, None) == B.PA_ERR_NULL
+    assert B.pa_prefill_f16(p, None, 512, 768, 1024, None, 4096, ws, stream=0) == B.PA_ERR_NULL
+    assert B.pa_prefill_f16(p, 256, 512, 768, None, None, 4096, ws, stream=0) == B.PA_ERR_NULL
+    assert B.pa_prefill_f16(p, 264, 512, 768, 1024, None, 4096, ws, stream=0) == B.PA_ERR_ALIGN
+    assert B.pa_prefill_f16(p, 256, 520, 768, 1024, None, 4096, ws, stream=0) == B.PA_ERR_ALIGN
+    assert B.pa_prefill_f16(p, 256, 512, 768, 1032, None, 4096, ws, stream=0) == B.PA_ERR_ALIGN
+    assert B.pa_prefill_f16(p, 256, 512, 768, 1024, 1026, 4096, ws, stream=0) == B.PA_ERR_ALIGN
+    assert B.pa_prefill_f16(p, 256, 512, 768, 1024, None, 4096, ws - 1, stream=0) == B.PA_ERR_WORKSPACE
+    assert B.pa_prefill_f16(p, 256, 512, 768, 1024, None, 4104, ws, stream=0) == B.PA_ERR_WORKSPACE
+    assert B.pa_prefill_f16(p, 256, 512, 768, 1024, None, None, ws, stream=0) == B.PA_ERR_WORKSPACE

@@ -1,0 +1,118 @@
+"""Causal prefill (pa_prefill_f16) against the FP64 oracle through the C ABI.
+
+Shapes follow "SM70 attention and quantized projection coverage across TP
+sizes", sections "Accumulation audit and rejected tuning" and "Graph replay
+and long-prefill follow-up" (Q8192 x KV262144, GQA 6, Hkv 1/2/4, B1/B2, FP16
+inputs); the small cases span several 128-query tiles, several key splits, a
+ragged last tile, strided K/V, contexts shorter than the query window and a
+single query.  The section "Additional findings" asks that batched multi-head
+calls match separate single-KV-head calls element for element; that is
+checked bitwise here."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import _compare, to_f64
+from oracle_pins import run_prefill_oracle
+from paged_gqa_decode_split_gb300 import binding as B
+from paged_gqa_decode_split_gb300 import build as pa_build
+from paged_gqa_decode_split_gb300 import workloads as wl
+from paged_gqa_decode_split_gb300.prefill import Prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pa_build.build()
+    B.load()
+
+
+def _visible(spec) -> np.ndarray:
+    """[B, q_len, Hq] bool: the query sees at least one key."""
+    i = np.arange(spec.q_len)
+    vis = spec.kv_len - spec.q_len + i >= 0
+    return np.broadcast_to(vis[None, :, None], (spec.batch, spec.q_len, spec.num_q_heads))
+
+
+def _run(w):
+    pf = Prefill(w)
+    pf.run()
+    torch.cuda.synchronize()
+    assert pf.status() == 0
+    return pf
+
+
+SMALL = [
+    # name, batch, q_len, kv_len, Hq, Hkv, token_pad
+    ("two_tiles_one_split", 1, 200, 1000, 6, 1, 0),
+    ("hkv2_strided_five_splits", 2, 300, 5000, 6, 2, 8),
+    ("context_shorter_than_queries", 1, 130, 100, 3, 1, 0),
+    ("square_causal", 1, 128, 128, 6, 1, 0),
+    ("single_query_three_splits", 1, 1, 70000, 6, 1, 0),
+    ("ragged_tiles_g4", 2, 257, 2113, 8, 2, 0),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_prefill_small_against_oracle(case):
+    name, b, q, kv, hq, hkv, pad = case
+    spec = wl.PrefillSpec(name, b, q, kv, hq, hkv, token_pad=pad)
+    w = wl.generate_prefill(spec, 40 + len(name), device="cuda")
+    pf = _run(w)
+    ref, rlse = run_prefill_oracle(w)
+    _compare(to_f64(pf.out), ref, _visible(spec), pf.lse, rlse)
+
+
+def _sample_rows(spec, rng, per_head=6):
+    rows = set()
+    Q, Hq = spec.q_len, spec.num_q_heads
+    for b in range(spec.batch):
+        for h in range(Hq):
+            qs = {0, Q - 1, min(127, Q - 1), min(128, Q - 1)} | set(rng.integers(0, Q, per_head).tolist())
+            rows |= {(b * Q + i) * Hq + h for i in qs}
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", ["prefill_q8192_kv262144"])
+def test_prefill_full_size_sampled(name):
+    spec = wl.PREFILL_SPECS[name]
+    w = wl.generate_prefill(spec, wl.PREFILL_SEED[name], device="cuda")
+    pf = _run(w)
+    rows = _sample_rows(spec, np.random.default_rng(5))
+    ref, rlse = run_prefill_oracle(w, rows=rows)
+    got = to_f64(pf.out).reshape(-1, spec.head_dim)[rows]
+    glse = pf.lse.reshape(-1)[torch.from_numpy(rows).long().cuda()]
+    vis = _visible(spec).reshape(-1)[rows]
+    _compare(got, ref, vis, glse, rlse)
+    assert torch.isfinite(pf.out).all()
+
+
+def test_prefill_batched_heads_equal_single_head_calls_bitwise():
+    """B2 x Hkv2 in one call equals four B1 x Hkv1 calls on the same rows."""
+    spec = wl.PrefillSpec("bitwise", 2, 300, 3000, 12, 2, token_pad=8)
+    w = wl.generate_prefill(spec, 77, device="cuda")
+    full = _run(w)
+    G = spec.num_q_heads // spec.num_kv_heads
+    for b in range(spec.batch):
+        for g in range(spec.num_kv_heads):
+            sub_spec = wl.PrefillSpec("one", 1, spec.q_len, spec.kv_len, G, 1, token_pad=spec.token_pad)
+            off_k = b * w.k_strides[0] + g * w.k_strides[2]
+            off_v = b * w.v_strides[0] + g * w.v_strides[2]
+            sub = wl.PrefillWorkload(spec=sub_spec, q=w.q[b:b + 1, :, g * G:(g + 1) * G].contiguous(),
+                                     k_buf=w.k_buf[off_k:], v_buf=w.v_buf[off_v:], k_strides=w.k_strides,
+                                     v_strides=w.v_strides)
+            one = _run(sub)
+            want = full.out[b:b + 1, :, g * G:(g + 1) * G]
+            assert torch.equal(one.out.view(torch.int16), want.contiguous().view(torch.int16)), (b, g)
+            assert torch.equal(one.lse, full.lse[b:b + 1, :, g * G:(g + 1) * G].contiguous()), (b, g)
+
+
+def test_prefill_repeat_is_bitwise_stable():
+    spec = wl.PrefillSpec("repeat", 1, 256, 40000, 6, 1)
+    w = wl.generate_prefill(spec, 78, device="cuda")
+    a = _run(w).out.clone()
+    b = _run(w).out
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
