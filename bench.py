@@ -47,6 +47,11 @@ NAMEPLATE_HBM_GBS = 8000.0  # GB300 HBM3e nameplate, for context next to the mea
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kernel_b8_l128k_traffic.json")
 
 
+def _progress(msg: str) -> None:
+    """A progress note on stderr (the JSON line goes to stdout)."""
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
@@ -439,6 +444,234 @@ def run_gpu(args, dist, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ prefill --
+PREFILL_METRIC = "logical causal TFLOP/s of the Q8192 x KV262144 causal prefill (FP16 in, FP32 accumulate)"
+
+
+def describe_prefill(spec) -> str:
+    return (f"causal prefill B{spec.batch}, {spec.q_len} queries (the last positions of a {spec.kv_len}-key "
+            f"context), Hq {spec.num_q_heads}, Hkv {spec.num_kv_heads} (GQA {spec.num_q_heads // spec.num_kv_heads}), "
+            f"D {spec.head_dim}, FP16 Q/K/V dense per request, FP32 accumulation")
+
+
+def _prefill_oracle_seconds(w_cpu, rows, nthreads):
+    import numpy as np
+    import torch
+
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    s = w_cpu.spec
+    t0 = time.perf_counter()
+    oracle.prefill_attn(q=bits(w_cpu.q), k=bits(w_cpu.k_buf), v=bits(w_cpu.v_buf), k_strides=w_cpu.k_strides,
+                        v_strides=w_cpu.v_strides, kv_len=s.kv_len, num_kv_heads=s.num_kv_heads,
+                        rows=np.asarray(rows, np.int32), num_threads=nthreads)
+    return time.perf_counter() - t0
+
+
+def _prefill_row_flops(spec, rows):
+    """Logical causal FLOPs of the listed flat rows (4 D per visible key)."""
+    total = 0
+    for r in rows:
+        i = (r // spec.num_q_heads) % spec.q_len
+        total += 4 * spec.head_dim * max(0, min(spec.kv_len, spec.kv_len - spec.q_len + i + 1))
+    return total
+
+
+def prefill_cpu_baseline(w_cpu, seconds_target=15.0):
+    import oracle
+
+    spec = w_cpu.spec
+    nthreads = oracle.max_threads()
+    # the last queries of every head (full contexts), one row per thread per round
+    rows_all = [((spec.q_len - 1 - k) * spec.num_q_heads + h) for k in range(spec.q_len) for h in range(spec.num_q_heads)]
+    t1 = _prefill_oracle_seconds(w_cpu, rows_all[:nthreads], nthreads)
+    rounds = max(1, min(len(rows_all) // nthreads, int(seconds_target / max(t1, 1e-3))))
+    _progress(f"oracle: {t1:.2f} s for {nthreads} rows on {nthreads} threads; sampling {rounds} rounds")
+    rows = rows_all[:rounds * nthreads]
+    t = _prefill_oracle_seconds(w_cpu, rows, nthreads)
+    return {"value": _prefill_row_flops(spec, rows) / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(rows)} of {spec.batch * spec.q_len * spec.num_q_heads} output rows (the last queries of "
+                      f"each head, full contexts), {t:.2f} s wall"}
+
+
+def run_reference_prefill(args, rank, world):
+    from paged_gqa_decode_split_gb300 import workloads as wl
+
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    spec = wl.PREFILL_SPECS[args.workload]
+    w = wl.generate_prefill(spec, wl.PREFILL_SEED[args.workload], device="cpu")
+    nthreads = oracle.max_threads()
+    rows = [((spec.q_len - 1) * spec.num_q_heads + h) % (spec.q_len * spec.num_q_heads) for h in range(nthreads)]
+    for _ in range(args.warmup):
+        _prefill_oracle_seconds(w, rows, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _prefill_oracle_seconds(w, rows, nthreads)
+    dt = time.perf_counter() - t0
+    value = _prefill_row_flops(spec, rows) * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe_prefill(spec), "global_batch": spec.batch, "seq_len": spec.kv_len,
+                       "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                             "sample": f"per step {len(rows)} output rows (last query of each head, full context)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _tensor_peak():
+    """(TFLOP/s, source): the measured sustained BF16 GEMM rate (FP16 has the
+    same nominal dense rate on this part), else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        for k in ("bf16_tflops_sustained", "bf16_tflops"):
+            if d.get(k):
+                return float(d[k]), f"measured {k} (FP16 dense rate = BF16 nominal)"
+    except Exception:
+        pass
+    return 1700.0, "fallback sustained BF16 (FP16 dense rate = BF16 nominal)"
+
+
+def run_gpu_prefill(args, dist, rank, world, local):
+    import torch
+
+    from paged_gqa_decode_split_gb300 import binding as B
+    from paged_gqa_decode_split_gb300 import build as pa_build
+    from paged_gqa_decode_split_gb300 import workloads as wl
+    from paged_gqa_decode_split_gb300.prefill import Prefill, logical_causal_flops
+
+    if rank == 0 or not pa_build.up_to_date():
+        pa_build.build()
+    if dist is not None:
+        dist.barrier()
+    B.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    spec = wl.PREFILL_SPECS[name]
+    seed = wl.PREFILL_SEED[name] + 1000 * rank
+    w = wl.generate_prefill(spec, seed, device=dev)
+    pf = Prefill(w)
+    flops = logical_causal_flops(spec.batch, spec.q_len, spec.kv_len, spec.num_q_heads, spec.head_dim)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        B.check(pf(stream), "warm-up call")
+    torch.cuda.synchronize(dev)
+    if pf.status() != 0:
+        raise RuntimeError(f"status flags {pf.status():#x} after warm-up")
+    _progress("warm-up done")
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
+    sampler.start()
+    time.sleep(0.3)
+    B.pa_timing_collect(0)
+    B.pa_timing_collect(1)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # attention-kernel events on every call (each call is milliseconds long)
+    B.pa_timing_enable(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        B.check(pf(stream), "timed call")
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    B.pa_timing_enable(False)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    st, k_ms, k_n = B.pa_timing_collect(1)
+    if pf.status() != 0:
+        raise RuntimeError(f"status flags {pf.status():#x} after the timed region")
+    _progress(f"timed region done: {ms / args.steps:.3f} ms per call")
+
+    # e2e: pinned host Q, K, V in; output and LSE out, every step
+    hq, hk, hv = w.q.cpu().pin_memory(), w.k_buf.cpu().pin_memory(), w.v_buf.cpu().pin_memory()
+    _progress("e2e host buffers pinned")
+    hout = torch.empty_like(hq).pin_memory()
+    hlse = torch.empty(tuple(hq.shape[:3]), dtype=torch.float32).pin_memory()
+    dw = wl.PrefillWorkload(spec=spec, q=torch.empty_like(w.q), k_buf=torch.empty_like(w.k_buf),
+                            v_buf=torch.empty_like(w.v_buf), k_strides=w.k_strides, v_strides=w.v_strides)
+    e2e_pf = Prefill(dw)
+    h2d = hq.nbytes + hk.nbytes + hv.nbytes
+    d2h = hout.nbytes + hlse.nbytes
+
+    def e2e_step():
+        dw.q.copy_(hq, non_blocking=True)
+        dw.k_buf.copy_(hk, non_blocking=True)
+        dw.v_buf.copy_(hv, non_blocking=True)
+        B.check(e2e_pf(stream), "e2e call")
+        hout.copy_(e2e_pf.out, non_blocking=True)
+        hlse.copy_(e2e_pf.lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    _progress("e2e warm-up step done")
+    e_steps = max(3, min(args.e2e_steps, 10))
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if not torch.equal(hout.to(dev).view(torch.int16), pf.out.view(torch.int16)):
+        raise RuntimeError("e2e output differs from the device-resident call")
+    _progress(f"e2e done: {e2e_s / e_steps * 1e3:.1f} ms per step")
+    del dw, e2e_pf
+    ms, e2e_s = reduce_max([ms, e2e_s], dist)
+    if rank != 0:
+        return
+    peak, peak_src = _tensor_peak()
+    kv_bytes = hk.nbytes + hv.nbytes
+    l2_note = (f"no flush: K and V ({kv_bytes / 1e6:.0f} MB) exceed the 129 MB L2" if kv_bytes > 129e6 else
+               f"K and V ({kv_bytes / 1e6:.0f} MB) fit in L2")
+    value = flops * args.steps * world / (ms / 1e3) / 1e12
+    k_avg_s = k_ms / max(k_n, 1) / 1e3
+    achieved = flops / k_avg_s / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        del w, pf
+        torch.cuda.empty_cache()
+        cpu = prefill_cpu_baseline(wl.generate_prefill(spec, seed, device=dev).to("cpu"))
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16->f32", "data": "synthetic",
+        "config": {"workload": describe_prefill(spec), "global_batch": spec.batch * world, "seq_len": spec.kv_len,
+                   "q_len": spec.q_len, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "logical_causal_flops_per_call": flops,
+                   "l2": l2_note},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": "prefill attention kernel (tcgen05, FP32 accumulate), without its merge kernel",
+                     "kernel_avg_us": k_avg_s * 1e6, "timed_launches": k_n,
+                     "algorithmic_flops_per_launch": flops,
+                     "timing": "CUDA events around the attention kernel of every timed call"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": flops * e_steps * world / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "note": "pinned host -> device copy of Q, K and V, the call, and a device -> host read of the "
+                        "output and LSE, synchronised every step"},
+        "cpu_baseline": cpu,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,10 +689,11 @@ def main():
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     dist, rank, world, local = _dist()
+    prefill = args.workload.startswith("prefill_")
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_reference_prefill if prefill else run_reference)(args, rank, world)
     else:
-        run_gpu(args, dist, rank, world, local)
+        (run_gpu_prefill if prefill else run_gpu)(args, dist, rank, world, local)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -216,6 +216,10 @@ __device__ void pf_mma(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb
 // when its max exceeds m by 2^kPfTau (then O, after PV(j-1), and l are
 // scaled by 2^(m_old - m_new)); write P = 2^(x - m) in FP16 and add it to l.
 // After the item's last PV: the row's partial (O, m, l) to global memory.
+// The TMEM loads and stores are warp-wide instructions, so every decision
+// that leads to one is taken by the whole warp: a rescale runs for all 32
+// rows when any of them needs it (the others with the factor 1, which leaves
+// their bits unchanged), and a failed wait on any lane ends the whole warp.
 __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, uint32_t tb) {
   WaitCtl* ctl = &M.ctl;
   const int r = warp * 32 + lane;
@@ -231,7 +235,7 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
     const long long vis_end = lim < x.k1 ? lim : x.k1;
     float m_ref = kPfNoMax, l = 0.0f;
     for (int j = 0; j < x.nt; ++j, ++jg) {
-      if (!mbar_wait(&M.s_full[jg & 1], (jg >> 1) & 1, ctl)) return;
+      if (!__all_sync(0xffffffffu, mbar_wait(&M.s_full[jg & 1], (jg >> 1) & 1, ctl))) return;
       tc_fence_after();
       const uint32_t s_addr = lane_base + kPfColS + (jg & 1) * 128;
       uint32_t u[128];
@@ -264,12 +268,13 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
         }
       }
       const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const bool up = j > 0 && mt > m_ref + kPfTau;
       if (j == 0) {
         m_ref = fmaxf(mt, kPfNoMax);
-      } else if (mt > m_ref + kPfTau) {
-        const float alpha = ex2_approx(m_ref - mt);
+      } else if (__any_sync(0xffffffffu, up)) {
+        const float alpha = up ? ex2_approx(m_ref - mt) : 1.0f;
         // O holds PV(0 .. j-1) once PV(j-1) has completed
-        if (!mbar_wait(&M.pv_done[(jg - 1) & 1], ((jg - 1) >> 1) & 1, ctl)) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(&M.pv_done[(jg - 1) & 1], ((jg - 1) >> 1) & 1, ctl))) return;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 16; ++c) {
@@ -279,8 +284,10 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
           for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           PA_TMEM_ST_X16(lane_base + kPfColO + 16 * c, o);
         }
-        l *= alpha;
-        m_ref = mt;
+        if (up) {
+          l *= alpha;
+          m_ref = mt;
+        }
       }
       uint32_t pk[64];
       float l0 = 0.0f, l1 = 0.0f;
@@ -301,7 +308,7 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
       if (lane == 0) mbar_arrive(&M.p_full[jg & 1]);
     }
     // epilogue: the row's partial, then O is free for the next item
-    if (!mbar_wait(&M.o_full, n & 1, ctl)) return;
+    if (!__all_sync(0xffffffffu, mbar_wait(&M.o_full, n & 1, ctl))) return;
     tc_fence_after();
     const size_t pidx = (((size_t)x.b * a.Hq + x.h) * a.n_qt + x.qt) * a.num_splits + x.s;
     float4* po = reinterpret_cast<float4*>(a.part_o + (pidx * kPfRows + r) * 256);

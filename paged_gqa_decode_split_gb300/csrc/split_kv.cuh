@@ -42,7 +42,9 @@
 //         rows: masking, lazy-max online softmax, P^T, row sums, O^T rescale,
 //         and the item's FP32 (m, l, O) partials written to the workspace.
 // Every wait is bounded (see mbar_wait); a wait that runs out aborts the CTA
-// cleanly, frees TMEM and raises PA_FLAG_TIMEOUT.
+// cleanly, frees TMEM and raises PA_FLAG_TIMEOUT.  A warp whose lanes all wait
+// on a barrier takes the outcome as a warp (any lane's failure ends all of
+// them), so no warp-wide TMEM instruction runs with part of a warp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -616,7 +618,7 @@ __device__ __forceinline__ void role_q_qk(const SplitArgs& a, Misc& M, int lane,
   for (int it = blockIdx.x, n = 0; ok && it < M.sched.total; it += gridDim.x, ++n) {
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
-    if (!mbar_wait(&M.q_empty, (n & 1) ^ 1, abort)) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&M.q_empty, (n & 1) ^ 1, abort))) break;
     if (a.q_tma) {
       // one box per 64-column atom: rows (qi, hl) land at r = qi * G + hl
       if (lane == 0 && !a.withhold_q) {  // withheld only by the timeout test hook
@@ -685,7 +687,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
     for (int jl = 0; jl < nt; ++jl, ++j) {
 #pragma unroll
       for (int h = 0; h < Fmt::kFills; ++h, ++f) {
-        if (!mbar_wait(&M.kst_full, f & 1, abort)) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(&M.kst_full, f & 1, abort))) return;
         // take this key's 256 staged row bytes into registers and hand the
         // stage back at once, so the loader's refill does not wait for the
         // tensor core
@@ -694,7 +696,8 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.kst_empty);
         // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
-        if (h == 0 && j >= 2 && !mbar_wait(&M.s_full[j & 1], ((j >> 1) & 1) ^ 1, abort)) return;
+        if (h == 0 && j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&M.s_full[j & 1], ((j >> 1) & 1) ^ 1, abort)))
+          return;
         const uint32_t taddr = tb + ((uint32_t)(32 * i) << 16) + kColK + (j & 1) * 128 + h * 64;
         if constexpr (Fmt::kElemBytes == 1) {
 #pragma unroll
@@ -746,7 +749,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
       const int slot = (int)(c % L::kVSlots);
 #pragma unroll
       for (int h = 0; h < Fmt::kFills; ++h, ++f) {
-        if (!mbar_wait(&M.vst_full, f & 1, abort)) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(&M.vst_full, f & 1, abort))) return;
         // row into registers, stage back to the loader, then wait for the slot
         uint4 raw[16];
         load_row<Win>(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
@@ -755,7 +758,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
         if (h == 0 && c >= (uint32_t)L::kVSlots) {
           // the slot's previous quarter belongs to tile t; PV(t) done frees it
           const uint32_t t = (c - L::kVSlots) / 4;
-          if (!mbar_wait(&M.pv_done[t % kPBufs], (t / kPBufs) & 1, abort)) return;
+          if (!__all_sync(0xffffffffu, mbar_wait(&M.pv_done[t % kPBufs], (t / kPBufs) & 1, abort))) return;
         }
         uint8_t* dst0 = vring + slot * L::kVQuarter + lane * 128;
 #pragma unroll

@@ -271,6 +271,10 @@ class PrefillWorkload:
     k_strides: tuple[int, int, int]  # (batch, token, head) in elements
     v_strides: tuple[int, int, int]
 
+    def to(self, device) -> "PrefillWorkload":
+        return dataclasses.replace(self, q=self.q.to(device), k_buf=self.k_buf.to(device),
+                                   v_buf=self.v_buf.to(device))
+
     def key_view(self, which: str) -> torch.Tensor:
         """[B][kv_len][Hkv][D] strided view of K or V."""
         s = self.spec
@@ -284,7 +288,9 @@ PREFILL_SPECS = {
     # the TP2 / TP1 local geometries, B2 (the bitwise per-head check's shapes)
     "prefill_q8192_kv262144_hkv2_b2": PrefillSpec("prefill_q8192_kv262144_hkv2_b2", 2, 8192, 262144, 12, 2),
 }
-PREFILL_SEED = {"prefill_q8192_kv262144": 2001, "prefill_q8192_kv262144_hkv2_b2": 2002}
+# a smaller case of the same kernel for profiler captures (K and V still exceed L2)
+PREFILL_SPECS["prefill_q2048_kv131072"] = PrefillSpec("prefill_q2048_kv131072", 1, 2048, 131072, 6, 1)
+PREFILL_SEED = {"prefill_q8192_kv262144": 2001, "prefill_q8192_kv262144_hkv2_b2": 2002, "prefill_q2048_kv131072": 2003}
 
 
 def generate_prefill(spec: PrefillSpec, seed: int, device: str | torch.device = "cpu") -> PrefillWorkload:

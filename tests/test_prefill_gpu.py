@@ -23,6 +23,10 @@ from paged_gqa_decode_split_gb300.prefill import Prefill
 
 pytestmark = pytest.mark.gpu
 
+# element bound for outputs dominated by a few keys: 2e-3 + 2^-10 |ref| (FP16
+# output rounding and the FP16 weight of the dominant key, 2^-11 each)
+DOMINANT_REL = 2.0 ** -10
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
@@ -116,3 +120,33 @@ def test_prefill_repeat_is_bitwise_stable():
     a = _run(w).out.clone()
     b = _run(w).out
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_prefill_growing_scores_force_rescales():
+    """Scores that grow along the keys at a different rate per query row move
+    the reference max of some rows of a warp and not of others, tile after
+    tile: the rescale of O runs warp-wide with factor 1 for the rows whose
+    max stays."""
+    spec = wl.PrefillSpec("growing", 1, 256, 4096, 6, 1)
+    w = wl.generate_prefill(spec, 79, device="cuda")
+    k = w.key_view("k")
+    growth = 1.0 + 6.0 * torch.arange(spec.kv_len, device="cuda", dtype=torch.float32) / spec.kv_len
+    k.copy_((k.float() * growth[None, :, None, None]).half())
+    row_scale = torch.linspace(0.25, 3.0, spec.q_len, device="cuda")[None, :, None, None]
+    w.q.copy_((w.q.float() * row_scale).half())
+    pf = _run(w)
+    ref, rlse = run_prefill_oracle(w)
+    _compare(to_f64(pf.out), ref, _visible(spec), pf.lse, rlse, rel_elem=DOMINANT_REL)
+
+
+def test_prefill_large_magnitude_inputs():
+    """Q and K ~ N(0, 8^2): scores in the tens to hundreds, softmax weights
+    concentrated on a few keys, frequent max moves."""
+    spec = wl.PrefillSpec("large", 1, 200, 3000, 6, 1)
+    w = wl.generate_prefill(spec, 80, device="cuda")
+    w.q.mul_(8.0)
+    w.key_view("k").mul_(8.0)
+    pf = _run(w)
+    assert torch.isfinite(pf.out).all()
+    ref, rlse = run_prefill_oracle(w)
+    _compare(to_f64(pf.out), ref, _visible(spec), pf.lse, rlse, rel_elem=DOMINANT_REL)
