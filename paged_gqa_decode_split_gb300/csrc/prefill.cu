@@ -18,11 +18,12 @@
 // The split length depends on kv_len alone, so a row's bits do not depend
 // on the batch or head count.
 //
-// Roles (192 threads):
+// Roles (224 threads):
 //   warps 0-3  softmax: thread = query row = TMEM lane; O rescale; epilogue
 //   warp 4     TMA loader (one thread): the item's Q tile, then K and V
 //              pieces of 16 KB into a ring, in the order they are consumed
-//   warp 5     TMEM allocation and the MMA issuer (one thread)
+//   warp 5     TMEM allocation and the QK issuer (one thread)
+//   warp 6     the PV issuer (one thread)
 // TMEM (512 columns): S double buffer at columns 0 and 128 (128 rows x 128
 // keys, FP32); P(j) in FP16, two keys per column, overwrites the first 64
 // columns of its S buffer; O at column 256 (128 rows x 256 d, FP32).
@@ -30,10 +31,8 @@
 //                      K-major), M 128, N 128, 16 steps of K 16 over d
 //   O    += P(j) V(j)  A = P (TMEM), B = V piece (shared, MN-major), M 128,
 //                      N 256, 8 steps of K 16 over keys
-// Issue order per item: QK(0), QK(1), PV(0), QK(2), PV(1), ..., PV(nt-1): the
-// tensor core computes S(j+1) while the softmax works on S(j); MMAs from one
-// thread run in issue order, so QK(j+2) overwrites S/P(j) only after PV(j)
-// has read P(j).
+// The tensor core computes S(j+1) while the softmax works on S(j); QK(j+2)
+// overwrites S/P(j) only after PV(j) has completed.
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -44,7 +43,7 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 224;
 constexpr int kPfRows = 128;      // queries per tile (M)
 constexpr int kPfKeys = 128;      // keys per tile
 constexpr int kPfRing = 10;       // ring pieces
@@ -57,7 +56,7 @@ constexpr uint32_t kPfColO = 256;
 
 struct PfBars {
   uint64_t full[kPfRing], empty[kPfRing];
-  uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, fin;
+  uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, fin_qk, fin_pv;
   uint32_t tmem_base;
   WaitCtl ctl;
 };
@@ -140,29 +139,40 @@ __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
   }
 }
 
-// MMA issuer (one thread).  Each ring piece is released by a commit after
-// the products that read it.
-__device__ void pf_mma(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
+// Fill index (within an item whose first piece is fill f0) of the first
+// piece of K(j) and of V(j): the loader issues K(0), then per tile j K(j+1)
+// (if any) and V(j), four pieces each.
+__device__ __forceinline__ uint32_t pf_fill_k(uint32_t f0, int j) { return j == 0 ? f0 : f0 + 8u * j - 4u; }
+__device__ __forceinline__ uint32_t pf_fill_v(uint32_t f0, int j, int nt) {
+  return j + 1 < nt ? f0 + 8u * (j + 1) : f0 + 8u * nt - 4u;
+}
+
+// QK issuer (one thread): S(j) = Q K(j)^T over 4 pieces (d atoms) of 4
+// steps each.  S(j) and P(j-2) share TMEM columns, so QK(j) waits until
+// PV(j-2) has completed.  Each ring piece is released by a commit after the
+// products that read it.  The two issuers run on separate threads so that
+// their instruction streams overlap (one thread issues an MMA every 100 or
+// so cycles, slower than the tensor core runs these shapes).
+__device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
   constexpr uint32_t id_qk = idesc_f16(128, 128, 0, 0, 0);
-  constexpr uint32_t id_pv = idesc_f16(128, 256, 0, 0, 1);
   WaitCtl* ctl = &M.ctl;
   const uint64_t q_desc = sdesc_sw128(smem_u32(sm + kPfOffQ), 16, 1024);
   const uint32_t ring0 = smem_u32(sm + kPfOffRing);
-  uint32_t f = 0, jg = 0;  // pieces consumed, tiles started (all items)
-  int n = 0;               // items started
+  uint32_t f0 = 0, jg = 0;  // first fill of the item, tiles of earlier items
+  int n = 0;                // items started
   for (int it = blockIdx.x; it < a.total_items; it += gridDim.x) {
     const PfItem x = pf_item(a, it);
     if (x.nt == 0) continue;
     if (!mbar_wait(&M.q_full, n & 1, ctl)) return;
     tc_fence_after();
-    const uint32_t j0 = jg;
-    // S(j) = Q K(j)^T: 4 pieces (d atoms) of 4 steps each
-    auto qk = [&](int j) -> bool {
-      const uint32_t jj = j0 + j;
+    for (int j = 0; j < x.nt; ++j) {
+      const uint32_t jj = jg + j;
+      if (jj >= 2 && !mbar_wait(&M.pv_done[jj & 1], ((jj - 2) >> 1) & 1, ctl)) return;
       const uint32_t s_col = tb + kPfColS + (jj & 1) * 128;
+      const uint32_t fk = pf_fill_k(f0, j);
       for (int at = 0; at < 4; ++at) {
-        const uint32_t slot = f % kPfRing, use = f / kPfRing;
-        if (!mbar_wait(&M.full[slot], use & 1, ctl)) return false;
+        const uint32_t idx = fk + at, slot = idx % kPfRing, use = idx / kPfRing;
+        if (!mbar_wait(&M.full[slot], use & 1, ctl)) return;
         tc_fence_after();
         const uint64_t k_desc = sdesc_sw128(ring0 + slot * kPfPiece, 16, 1024);
 #pragma unroll
@@ -170,23 +180,38 @@ __device__ void pf_mma(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb
           mma_ss(s_col, sdesc_add(q_desc, at * 16384 + kk * 32), sdesc_add(k_desc, kk * 32), id_qk,
                  (at | kk) != 0 ? 1u : 0u);
         mma_commit(&M.empty[slot]);
-        ++f;
       }
       mma_commit(&M.s_full[jj & 1]);
       if (j == x.nt - 1) mma_commit(&M.q_empty);
-      return true;
-    };
-    // O += P(j) V(j): 4 pieces (32 keys) of 2 steps each; the item's first
-    // product overwrites O once the previous item's epilogue has read it
-    auto pv = [&](int j) -> bool {
-      const uint32_t jj = j0 + j;
-      if (!mbar_wait(&M.p_full[jj & 1], (jj >> 1) & 1, ctl)) return false;
-      if (j == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, ctl)) return false;
+    }
+    f0 += 8u * x.nt;
+    jg += x.nt;
+    ++n;
+  }
+}
+
+// PV issuer (one thread): O += P(j) V(j) over 4 pieces (32 keys) of 2 steps
+// each, once the softmax has written P(j); an item's first product
+// overwrites O once the previous item's epilogue has read it.
+__device__ void pf_mma_pv(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
+  constexpr uint32_t id_pv = idesc_f16(128, 256, 0, 0, 1);
+  WaitCtl* ctl = &M.ctl;
+  const uint32_t ring0 = smem_u32(sm + kPfOffRing);
+  uint32_t f0 = 0, jg = 0;
+  int n = 0;
+  for (int it = blockIdx.x; it < a.total_items; it += gridDim.x) {
+    const PfItem x = pf_item(a, it);
+    if (x.nt == 0) continue;
+    for (int j = 0; j < x.nt; ++j) {
+      const uint32_t jj = jg + j;
+      if (!mbar_wait(&M.p_full[jj & 1], (jj >> 1) & 1, ctl)) return;
+      if (j == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, ctl)) return;
       tc_fence_after();
       const uint32_t p_col = tb + kPfColS + (jj & 1) * 128;
+      const uint32_t fv = pf_fill_v(f0, j, x.nt);
       for (int pc = 0; pc < 4; ++pc) {
-        const uint32_t slot = f % kPfRing, use = f / kPfRing;
-        if (!mbar_wait(&M.full[slot], use & 1, ctl)) return false;
+        const uint32_t idx = fv + pc, slot = idx % kPfRing, use = idx / kPfRing;
+        if (!mbar_wait(&M.full[slot], use & 1, ctl)) return;
         tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(ring0 + slot * kPfPiece, 4096, 1024);
 #pragma unroll
@@ -194,17 +219,11 @@ __device__ void pf_mma(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb
           mma_ts(tb + kPfColO, p_col + (2 * pc + kk) * 8, sdesc_add(v_desc, kk * 2048), id_pv,
                  (j > 0 || pc > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&M.empty[slot]);
-        ++f;
       }
       mma_commit(&M.pv_done[jj & 1]);
       if (j == x.nt - 1) mma_commit(&M.o_full);
-      return true;
-    };
-    if (!qk(0)) return;
-    for (int j = 0; j < x.nt; ++j) {
-      if (j + 1 < x.nt && !qk(j + 1)) return;
-      if (!pv(j)) return;
     }
+    f0 += 8u * x.nt;
     jg += x.nt;
     ++n;
   }
@@ -347,7 +366,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
     mbar_init(&M.o_full, 1);
     mbar_init(&M.o_free, 4);
-    mbar_init(&M.fin, 1);
+    mbar_init(&M.fin_qk, 1);
+    mbar_init(&M.fin_pv, 1);
     M.ctl.abort = 0;
     M.ctl.limit = a.wait_limit > 0 ? a.wait_limit : kWaitLimitCycles;
     mbar_fence_init();
@@ -363,12 +383,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   } else if (warp == 4) {
     if (lane == 0) pf_loader(a, M, sm);
     __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      pf_mma_qk(a, M, sm, tb);
+      // every product this thread issued completes before TMEM is released
+      mma_commit(&M.fin_qk);
+      mbar_drain(&M.fin_qk, 0, &M.ctl);
+    }
+    __syncwarp();
   } else {
     if (lane == 0) {
-      pf_mma(a, M, sm, tb);
-      // every product this thread issued completes before TMEM is released
-      mma_commit(&M.fin);
-      mbar_drain(&M.fin, 0, &M.ctl);
+      pf_mma_pv(a, M, sm, tb);
+      mma_commit(&M.fin_pv);
+      mbar_drain(&M.fin_pv, 0, &M.ctl);
     }
     __syncwarp();
   }
