@@ -192,6 +192,8 @@ struct Layout {
   static_assert(kStageAlloc % 1024 == 0, "staging tiles must keep the 1024-byte swizzle alignment");
   static_assert(kVSlots >= 4, "the V' ring must hold a whole tile");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory map exceeds the per-block limit");
+  // the merge phase stages each worker's split partials below Misc
+  static_assert((kThreads / 128) * kMaxSplits * 128 * 4 <= kOffMisc, "merge staging overlaps Misc");
 };
 
 // Cross-lane reduction of n per-lane values (one per packed row) in a warp.
@@ -1137,13 +1139,13 @@ __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid
     const int qi = row / a.G, hl = row % a.G;
     const size_t orow = (size_t)(b * a.q_len + qi) * a.Hq + g * a.G + hl;
     const size_t prow = (size_t)(b * a.Hkv + g) * a.s_max * a.R + row;  // panel row of split 0; split s at + s * R
-    // the partial O of every split, requested before the weights are known so
-    // that the two rounds of loads overlap
+    // the partial O of every split into the worker's area of the (now idle)
+    // pipeline shared memory, requested before the weights are known so that
+    // the two rounds of loads overlap; element (s, e) at stage[s * 128 + e]
     const float* o0 = a.panel_o + prow * Fmt::D + d;
     const size_t sstride = (size_t)a.R * Fmt::D;
-    float o[kMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) o[s] = s < ns ? __ldcg(o0 + s * sstride) : 0.f;
+    const uint32_t stage = smem_u32(smem_base()) + (uint32_t)(w * kMaxSplits * 128 + e) * 4u;
+    for (int s = 0; s < ns; ++s) cp_async_4(stage + (uint32_t)s * 512u, o0 + s * sstride);
     // one warp, splits s and s + 32 on lane s: M = max_s m_s, w_s = 2^(m_s - M),
     // lsum = sum_s w_s l_s (a fixed reduction tree, so the bits depend on ns only)
     if (e < 32) {
@@ -1174,13 +1176,14 @@ __device__ __forceinline__ void merge_phase(const SplitArgs& a, Misc& M, int tid
       }
     }
     named_bar_sync(bar, 128);
+    cp_async_wait_all();  // this thread's own partials (it reads no other thread's)
     const float lsum = M.clsum[w];
     float val = 0.f;
     if (lsum > 0.f) {
       // accumulation in ascending split order
+      const float* so = reinterpret_cast<const float*>(smem_base()) + w * kMaxSplits * 128 + e;
       float acc = 0.f;
-#pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s) acc = (s < ns) ? fmaf(M.cw[w][s], o[s], acc) : acc;
+      for (int s = 0; s < ns; ++s) acc = fmaf(M.cw[w][s], so[s * 128], acc);
       val = acc / lsum * scale;
     }
     if constexpr (Fmt::kQBf16) {
