@@ -43,8 +43,11 @@
 //         and the item's FP32 (m, l, O) partials written to the workspace.
 // Every wait is bounded (see mbar_wait); a wait that runs out aborts the CTA
 // cleanly, frees TMEM and raises PA_FLAG_TIMEOUT.  A warp whose lanes all wait
-// on a barrier takes the outcome as a warp (any lane's failure ends all of
-// them), so no warp-wide TMEM instruction runs with part of a warp.
+// on a barrier leaves as a warp (any lane's failure ends all of them), so no
+// warp-wide instruction runs with part of a warp: the decode warps finish the
+// tile they are in (after an abort the data no longer matters) and vote once
+// at its end, where the warp is converged; a vote at every wait costs about
+// 2 % of the kernel's time.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -687,9 +690,10 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
     const Item x = sched_item(M.sched, a.B, it);
     const int nt = tiles_of(x);
     for (int jl = 0; jl < nt; ++jl, ++j) {
+      bool ok = true;  // every wait of this tile succeeded (the warp decides at the tile's end)
 #pragma unroll
       for (int h = 0; h < Fmt::kFills; ++h, ++f) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&M.kst_full, f & 1, abort))) return;
+        ok = mbar_wait(&M.kst_full, f & 1, abort) && ok;
         // take this key's 256 staged row bytes into registers and hand the
         // stage back at once, so the loader's refill does not wait for the
         // tensor core
@@ -698,8 +702,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.kst_empty);
         // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
-        if (h == 0 && j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&M.s_full[j & 1], ((j >> 1) & 1) ^ 1, abort)))
-          return;
+        if (h == 0 && j >= 2) ok = mbar_wait(&M.s_full[j & 1], ((j >> 1) & 1) ^ 1, abort) && ok;
         const uint32_t taddr = tb + ((uint32_t)(32 * i) << 16) + kColK + (j & 1) * 128 + h * 64;
         if constexpr (Fmt::kElemBytes == 1) {
 #pragma unroll
@@ -726,6 +729,7 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.kbuf_full[j & 1]);
+      if (__any_sync(0xffffffffu, !ok)) return;
     }
   }
 }
@@ -749,9 +753,10 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
     for (int jl = 0; jl < nt; ++jl, ++j) {
       const uint32_t c = 4 * j + i;
       const int slot = (int)(c % L::kVSlots);
+      bool ok = true;  // every wait of this tile succeeded (the warp decides at the tile's end)
 #pragma unroll
       for (int h = 0; h < Fmt::kFills; ++h, ++f) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&M.vst_full, f & 1, abort))) return;
+        ok = mbar_wait(&M.vst_full, f & 1, abort) && ok;
         // row into registers, stage back to the loader, then wait for the slot
         uint4 raw[16];
         load_row<Win>(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
@@ -760,7 +765,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
         if (h == 0 && c >= (uint32_t)L::kVSlots) {
           // the slot's previous quarter belongs to tile t; PV(t) done frees it
           const uint32_t t = (c - L::kVSlots) / 4;
-          if (!__all_sync(0xffffffffu, mbar_wait(&M.pv_done[t % kPBufs], (t / kPBufs) & 1, abort))) return;
+          ok = mbar_wait(&M.pv_done[t % kPBufs], (t / kPBufs) & 1, abort) && ok;
         }
         uint8_t* dst0 = vring + slot * L::kVQuarter + lane * 128;
 #pragma unroll
@@ -786,6 +791,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.vtile_full[j & 1]);
+      if (__any_sync(0xffffffffu, !ok)) return;
     }
   }
 }
