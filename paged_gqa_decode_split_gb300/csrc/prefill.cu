@@ -25,14 +25,15 @@
 //   warp 5     TMEM allocation and the QK issuer (one thread)
 //   warp 6     the PV issuer (one thread)
 // TMEM (512 columns): S double buffer at columns 0 and 128 (128 rows x 128
-// keys, FP32); P(j) in FP16, two keys per column, overwrites the first 64
-// columns of its S buffer; O at column 256 (128 rows x 256 d, FP32).
+// keys, FP32); O at column 256 (128 rows x 256 d, FP32).  Shared memory: Q
+// tile (64 KB), P double buffer (2 x 32 KB, FP16), ring of 6 K/V pieces.
 //   S(j)  = Q K(j)^T   A = Q (shared, K-major), B = K piece (shared,
 //                      K-major), M 128, N 128, 16 steps of K 16 over d
-//   O    += P(j) V(j)  A = P (TMEM), B = V piece (shared, MN-major), M 128,
-//                      N 256, 8 steps of K 16 over keys
-// The tensor core computes S(j+1) while the softmax works on S(j); QK(j+2)
-// overwrites S/P(j) only after PV(j) has completed.
+//   O    += P(j) V(j)  A = P (shared, K-major), B = V piece (shared,
+//                      MN-major), M 128, N 256, 8 steps of K 16 over keys
+// The tensor core computes S(j+1) and S(j+2) while the softmax works on
+// S(j): an S buffer is free again once the softmax has read it into
+// registers, and P has buffers of its own.
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -46,9 +47,10 @@ namespace {
 constexpr int kPfThreads = 224;
 constexpr int kPfRows = 128;      // queries per tile (M)
 constexpr int kPfKeys = 128;      // keys per tile
-constexpr int kPfRing = 10;       // ring pieces
+constexpr int kPfRing = 6;        // ring pieces
 constexpr int kPfPiece = 16384;   // one K piece (128 keys x 64 d) or V piece (32 keys x 256 d)
 constexpr int kPfQBytes = 65536;  // Q tile: 4 atoms of 128 queries x 64 d
+constexpr int kPfPBytes = 32768;  // one P buffer: 2 atoms of 128 queries x 64 keys (FP16)
 constexpr float kPfTau = 8.0f;    // the reference max moves only when a score exceeds it by 2^8
 constexpr float kPfNoMax = -1e30f;  // reference max of a row that has seen no key (finite, so 2^(x - m) is never NaN)
 constexpr uint32_t kPfColS = 0;
@@ -56,13 +58,14 @@ constexpr uint32_t kPfColO = 256;
 
 struct PfBars {
   uint64_t full[kPfRing], empty[kPfRing];
-  uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, fin_qk, fin_pv;
+  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, fin_qk, fin_pv;
   uint32_t tmem_base;
   WaitCtl ctl;
 };
 
 constexpr int kPfOffQ = 0;
-constexpr int kPfOffRing = kPfQBytes;
+constexpr int kPfOffP = kPfQBytes;
+constexpr int kPfOffRing = kPfOffP + 2 * kPfPBytes;
 constexpr int kPfOffBars = kPfOffRing + kPfRing * kPfPiece;
 constexpr int kPfSmem = kPfOffBars + (int)sizeof(PfBars) + 1024;  // + slack for the 1024-byte alignment
 static_assert(kPfSmem <= 232448, "prefill shared memory map exceeds the per-block limit");
@@ -95,9 +98,11 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& a, int it) {
 }
 
 // Loader: per item the Q tile (once every QK of the previous item has
-// completed), then the pieces in consumption order: K(0), and for each tile
-// j, K(j+1) (if any) and V(j).  K(j) = 4 pieces (d atoms), V(j) = 4 pieces
-// (32 keys each).  Keys past kv_len arrive as zeros (outside the view).
+// completed), then the pieces with K two tiles ahead of V: K(0), K(1), then
+// K(j), V(j-2) for j = 2 .. nt-1, then the last two V.  K(j) = 4 pieces (d
+// atoms), V(j) = 4 pieces (32 keys each).  With K ahead, the ring never
+// holds back QK(j+2) behind PV(j), which waits for the softmax.  Keys past
+// kv_len arrive as zeros (outside the view).
 __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
   WaitCtl* ctl = &M.ctl;
   const uint32_t ring0 = smem_u32(sm + kPfOffRing);
@@ -125,11 +130,14 @@ __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
       ++f;
       return true;
     };
-    for (int p = 0; ok && p < 4; ++p) ok = piece(false, 0, p);
-    for (int j = 0; ok && j < x.nt; ++j) {
-      for (int p = 0; ok && p < 4 && j + 1 < x.nt; ++p) ok = piece(false, j + 1, p);
-      for (int p = 0; ok && p < 4; ++p) ok = piece(true, j, p);
+    for (int j = 0; ok && j < 2 && j < x.nt; ++j)
+      for (int p = 0; ok && p < 4; ++p) ok = piece(false, j, p);
+    for (int j = 2; ok && j < x.nt; ++j) {
+      for (int p = 0; ok && p < 4; ++p) ok = piece(false, j, p);
+      for (int p = 0; ok && p < 4; ++p) ok = piece(true, j - 2, p);
     }
+    for (int j = x.nt > 2 ? x.nt - 2 : 0; ok && j < x.nt; ++j)
+      for (int p = 0; ok && p < 4; ++p) ok = piece(true, j, p);
     if (!ok) break;
   }
   if (ctl->abort) {
@@ -140,17 +148,19 @@ __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
 }
 
 // Fill index (within an item whose first piece is fill f0) of the first
-// piece of K(j) and of V(j): the loader issues K(0), then per tile j K(j+1)
-// (if any) and V(j), four pieces each.
-__device__ __forceinline__ uint32_t pf_fill_k(uint32_t f0, int j) { return j == 0 ? f0 : f0 + 8u * j - 4u; }
+// piece of K(j) and of V(j), in the loader's order K(0), K(1), [K(j),
+// V(j-2)] for j >= 2, V(nt-2), V(nt-1): four pieces each.
+__device__ __forceinline__ uint32_t pf_fill_k(uint32_t f0, int j) {
+  return j == 0 ? f0 : (j == 1 ? f0 + 4u : f0 + 8u * j - 8u);
+}
 __device__ __forceinline__ uint32_t pf_fill_v(uint32_t f0, int j, int nt) {
-  return j + 1 < nt ? f0 + 8u * (j + 1) : f0 + 8u * nt - 4u;
+  return j + 3 <= nt ? f0 + 12u + 8u * j : f0 + 8u * nt - 4u * (nt - j);
 }
 
 // QK issuer (one thread): S(j) = Q K(j)^T over 4 pieces (d atoms) of 4
-// steps each.  S(j) and P(j-2) share TMEM columns, so QK(j) waits until
-// PV(j-2) has completed.  Each ring piece is released by a commit after the
-// products that read it.  The two issuers run on separate threads so that
+// steps each, into S buffer j & 1 once the softmax has read S(j-2) out of
+// it.  Each ring piece is released by a commit after the products that read
+// it.  The two issuers run on separate threads so that
 // their instruction streams overlap (one thread issues an MMA every 100 or
 // so cycles, slower than the tensor core runs these shapes).
 __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
@@ -167,7 +177,7 @@ __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
     tc_fence_after();
     for (int j = 0; j < x.nt; ++j) {
       const uint32_t jj = jg + j;
-      if (jj >= 2 && !mbar_wait(&M.pv_done[jj & 1], ((jj - 2) >> 1) & 1, ctl)) return;
+      if (jj >= 2 && !mbar_wait(&M.s_free[jj & 1], ((jj - 2) >> 1) & 1, ctl)) return;
       const uint32_t s_col = tb + kPfColS + (jj & 1) * 128;
       const uint32_t fk = pf_fill_k(f0, j);
       for (int at = 0; at < 4; ++at) {
@@ -191,12 +201,14 @@ __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
 }
 
 // PV issuer (one thread): O += P(j) V(j) over 4 pieces (32 keys) of 2 steps
-// each, once the softmax has written P(j); an item's first product
-// overwrites O once the previous item's epilogue has read it.
+// each, P(j) from shared buffer j & 1 once the softmax has written it; an
+// item's first product overwrites O once the previous item's epilogue has
+// read it.
 __device__ void pf_mma_pv(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
   constexpr uint32_t id_pv = idesc_f16(128, 256, 0, 0, 1);
   WaitCtl* ctl = &M.ctl;
   const uint32_t ring0 = smem_u32(sm + kPfOffRing);
+  const uint32_t p0 = smem_u32(sm + kPfOffP);
   uint32_t f0 = 0, jg = 0;
   int n = 0;
   for (int it = blockIdx.x; it < a.total_items; it += gridDim.x) {
@@ -207,7 +219,7 @@ __device__ void pf_mma_pv(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
       if (!mbar_wait(&M.p_full[jj & 1], (jj >> 1) & 1, ctl)) return;
       if (j == 0 && !mbar_wait(&M.o_free, (n & 1) ^ 1, ctl)) return;
       tc_fence_after();
-      const uint32_t p_col = tb + kPfColS + (jj & 1) * 128;
+      const uint64_t p_desc = sdesc_sw128(p0 + (jj & 1) * kPfPBytes, 16, 1024);
       const uint32_t fv = pf_fill_v(f0, j, x.nt);
       for (int pc = 0; pc < 4; ++pc) {
         const uint32_t idx = fv + pc, slot = idx % kPfRing, use = idx / kPfRing;
@@ -215,9 +227,12 @@ __device__ void pf_mma_pv(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
         tc_fence_after();
         const uint64_t v_desc = sdesc_sw128(ring0 + slot * kPfPiece, 4096, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          mma_ts(tb + kPfColO, p_col + (2 * pc + kk) * 8, sdesc_add(v_desc, kk * 2048), id_pv,
+        for (int kk = 0; kk < 2; ++kk) {
+          // keys 32 pc + 16 kk .. +15: atom pc / 2, 32-byte step (2 pc + kk) % 4 within it
+          const uint32_t p_off = (uint32_t)(pc >> 1) * 16384u + (uint32_t)((2 * pc + kk) & 3) * 32u;
+          mma_ss(tb + kPfColO, sdesc_add(p_desc, p_off), sdesc_add(v_desc, kk * 2048), id_pv,
                  (j > 0 || pc > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(&M.empty[slot]);
       }
       mma_commit(&M.pv_done[jj & 1]);
@@ -230,16 +245,19 @@ __device__ void pf_mma_pv(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
 }
 
 // Softmax, one query row per thread (row r = TMEM lane r).  Per tile: load
-// the 128 scores, mask keys the row does not see, take the tile max; the
-// item's first tile sets the reference max m, a later tile moves it only
-// when its max exceeds m by 2^kPfTau (then O, after PV(j-1), and l are
-// scaled by 2^(m_old - m_new)); write P = 2^(x - m) in FP16 and add it to l.
-// After the item's last PV: the row's partial (O, m, l) to global memory.
+// the 128 scores and release the S buffer, mask keys the row does not see,
+// take the tile max; the item's first tile sets the reference max m, a later
+// tile moves it only when its max exceeds m by 2^kPfTau (then O, after
+// PV(j-1), and l are scaled by 2^(m_old - m_new)); write P = 2^(x - m) in
+// FP16 into shared P buffer j & 1 (once PV(j-2) has read it), K-major with
+// the 128-byte swizzle (row r's 16-byte chunk c of atom a at a * 16384 +
+// r * 128 + ((c ^ (r % 8)) * 16)), and add it to l.  After the item's last
+// PV: the row's partial (O, m, l) to global memory.
 // The TMEM loads and stores are warp-wide instructions, so every decision
 // that leads to one is taken by the whole warp: a rescale runs for all 32
 // rows when any of them needs it (the others with the factor 1, which leaves
 // their bits unchanged), and a failed wait on any lane ends the whole warp.
-__device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, uint32_t tb) {
+__device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, uint32_t tb, uint8_t* sm) {
   WaitCtl* ctl = &M.ctl;
   const int r = warp * 32 + lane;
   const uint32_t lane_base = tb + ((uint32_t)(warp * 32) << 16);
@@ -262,6 +280,10 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
       for (int c = 0; c < 8; ++c) PA_TMEM_LD_X16(s_addr + 16 * c, (u + 16 * c));
       tmem_wait_ld();
       reg_fence(u);
+      // S(j) is in registers: QK(j+2) may overwrite its buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.s_free[jg & 1]);
       const long long t0 = (long long)x.k0 + (long long)j * kPfKeys;
       const long long nv = vis_end - t0;
       const int nvis = nv <= 0 ? 0 : (nv >= kPfKeys ? kPfKeys : (int)nv);
@@ -319,9 +341,17 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
         pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       l += l0 + l1;
+      // P buffer jg & 1 is free once PV(jg-2) has completed
+      if (jg >= 2 && !__all_sync(0xffffffffu, mbar_wait(&M.pv_done[jg & 1], ((jg - 2) >> 1) & 1, ctl))) return;
+      uint8_t* prow = sm + kPfOffP + (jg & 1) * kPfPBytes + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) PA_TMEM_ST_X16(s_addr + 16 * c, (pk + 16 * c));
-      tmem_wait_st();
+      for (int a2 = 0; a2 < 2; ++a2)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + a2 * 16384 + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[32 * a2 + 4 * c], pk[32 * a2 + 4 * c + 1], pk[32 * a2 + 4 * c + 2], pk[32 * a2 + 4 * c + 3]);
+      tmem_wait_st();  // the O rescale's stores, if any
+      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&M.p_full[jg & 1]);
@@ -361,6 +391,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     mbar_init(&M.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&M.s_full[s], 1);
+      mbar_init(&M.s_free[s], 4);  // one arrival per softmax warp
       mbar_init(&M.p_full[s], 4);  // one arrival per softmax warp
       mbar_init(&M.pv_done[s], 1);
     }
@@ -379,7 +410,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const uint32_t tb = M.tmem_base;
 
   if (warp < 4) {
-    pf_softmax(a, M, warp, lane, tb);
+    pf_softmax(a, M, warp, lane, tb, sm);
   } else if (warp == 4) {
     if (lane == 0) pf_loader(a, M, sm);
     __syncwarp();
