@@ -389,7 +389,7 @@ PfLayout prefill_layout(const pa_prefill_params* p) {
 // multiple of 16 serves
 cuuint64_t pf_stride(long long elems, bool unit) { return unit ? 1024 : (cuuint64_t)elems * 2; }
 
-bool encode_prefill_maps(PrefillArgs* a, const pa_prefill_params* p, const void* q, const void* k, const void* v) {
+bool encode_prefill_maps(PrefillArgs* a, const pa_prefill_params* p, const void* k, const void* v) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
@@ -398,16 +398,6 @@ bool encode_prefill_maps(PrefillArgs* a, const pa_prefill_params* p, const void*
   const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   const auto oob = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE;
   const bool b1 = p->batch == 1, h1 = p->num_kv_heads == 1;
-  // Q: (d within atom, query, atom, head, request)
-  {
-    const cuuint64_t row = (cuuint64_t)p->num_q_heads * 512;
-    cuuint64_t dims[5] = {64, (cuuint64_t)p->q_len, 4, (cuuint64_t)p->num_q_heads, (cuuint64_t)p->batch};
-    cuuint64_t strides[4] = {row, 128, 512, b1 ? 1024 : row * (cuuint64_t)p->q_len};
-    cuuint32_t box[5] = {64, 128, 4, 1, 1};
-    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (enc(&a->q_map, f16, 5, const_cast<void*>(q), dims, strides, box, estr, il, sw, l2, oob) != CUDA_SUCCESS)
-      return false;
-  }
   // K: (d, KV head, key, request)
   {
     cuuint64_t dims[4] = {256, (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->kv_len, (cuuint64_t)p->batch};
@@ -449,7 +439,8 @@ int prefill_f16(const pa_prefill_params* p, const void* q, const void* k, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_prefill_maps(&a, p, q, k, v)) return PA_ERR_CUDA;
+  if (!encode_prefill_maps(&a, p, k, v)) return PA_ERR_CUDA;
+  a.q = q;
   a.part_ml = reinterpret_cast<float2*>(ws + L.ml_off);
   a.part_o = reinterpret_cast<float*>(ws + L.o_off);
   a.status = reinterpret_cast<uint32_t*>(ws);

@@ -67,14 +67,12 @@ struct SplitArgs {
 // it = ((s * B + b) * n_qt + qt) * Hq + h: query tile qt (128 queries) of
 // query head h of request b against key split s (split_len keys).
 struct PrefillArgs {
-  // Q [B][q_len][Hq][256]: 5-D view (d within a 64-column atom, query, atom,
-  // head, request), one box of 64 x 128 queries x 4 atoms = the whole tile
-  CUtensorMap q_map;
   // K: 4-D view (d, KV head, key, request), boxes of 64 d x 128 keys
   CUtensorMap k_map;
   // V: 5-D view (d within atom, key, atom, KV head, request), boxes of
   // 64 d x 32 keys x 4 atoms
   CUtensorMap v_map;
+  const void* q;    // FP16 [B][q_len][Hq][256], contiguous
   float* part_o;    // FP32 partial O per (item tile, row, d), unnormalised
   float2* part_ml;  // (m in log2 units, l) per (item tile, row)
   uint32_t* status;

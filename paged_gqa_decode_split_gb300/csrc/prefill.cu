@@ -19,21 +19,24 @@
 // on the batch or head count.
 //
 // Roles (224 threads):
-//   warps 0-3  softmax: thread = query row = TMEM lane; O rescale; epilogue
-//   warp 4     TMA loader (one thread): the item's Q tile, then K and V
-//              pieces of 16 KB into a ring, in the order they are consumed
+//   warps 0-3  softmax: thread = query row = TMEM lane; the item's Q rows
+//              into TMEM; O rescale; epilogue
+//   warp 4     TMA loader (one thread): K and V pieces of 16 KB into a
+//              ring, in the order they are consumed
 //   warp 5     TMEM allocation and the QK issuer (one thread)
 //   warp 6     the PV issuer (one thread)
-// TMEM (512 columns): S double buffer at columns 0 and 128 (128 rows x 128
-// keys, FP32); O at column 256 (128 rows x 256 d, FP32).  Shared memory: Q
-// tile (64 KB), P double buffer (2 x 32 KB, FP16), ring of 6 K/V pieces.
-//   S(j)  = Q K(j)^T   A = Q (shared, K-major), B = K piece (shared,
-//                      K-major), M 128, N 128, 16 steps of K 16 over d
+// TMEM (512 columns): the Q tile at columns 0-127 (FP16, two d per column),
+// S at 128 (128 rows x 128 keys, FP32), O at 256 (128 rows x 256 d, FP32).
+// Shared memory: P double buffer (2 x 32 KB, FP16), ring of 10 K/V pieces.
+//   S(j)  = Q K(j)^T   A = Q (TMEM), B = K piece (shared, K-major), M 128,
+//                      N 128, 16 steps of K 16 over d
 //   O    += P(j) V(j)  A = P (shared, K-major), B = V piece (shared,
 //                      MN-major), M 128, N 256, 8 steps of K 16 over keys
-// The tensor core computes S(j+1) and S(j+2) while the softmax works on
-// S(j): an S buffer is free again once the softmax has read it into
-// registers, and P has buffers of its own.
+// The tensor core computes S(j+1) while the softmax works on S(j): S is free
+// again once the softmax has read it into registers, and P has buffers of
+// its own.  With Q in TMEM the QK products read only K from shared memory;
+// the shared-memory traffic (TMA writes of K and V, P writes, operand reads)
+// is what bounds this kernel.
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -47,24 +50,23 @@ namespace {
 constexpr int kPfThreads = 224;
 constexpr int kPfRows = 128;      // queries per tile (M)
 constexpr int kPfKeys = 128;      // keys per tile
-constexpr int kPfRing = 6;        // ring pieces
+constexpr int kPfRing = 10;       // ring pieces
 constexpr int kPfPiece = 16384;   // one K piece (128 keys x 64 d) or V piece (32 keys x 256 d)
-constexpr int kPfQBytes = 65536;  // Q tile: 4 atoms of 128 queries x 64 d
 constexpr int kPfPBytes = 32768;  // one P buffer: 2 atoms of 128 queries x 64 keys (FP16)
 constexpr float kPfTau = 8.0f;    // the reference max moves only when a score exceeds it by 2^8
 constexpr float kPfNoMax = -1e30f;  // reference max of a row that has seen no key (finite, so 2^(x - m) is never NaN)
-constexpr uint32_t kPfColS = 0;
+constexpr uint32_t kPfColQ = 0;
+constexpr uint32_t kPfColS = 128;
 constexpr uint32_t kPfColO = 256;
 
 struct PfBars {
   uint64_t full[kPfRing], empty[kPfRing];
-  uint64_t q_full, q_empty, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, fin_qk, fin_pv;
+  uint64_t q_full, s_full, s_free, p_full[2], pv_done[2], o_full, o_free, fin_qk, fin_pv;
   uint32_t tmem_base;
   WaitCtl ctl;
 };
 
-constexpr int kPfOffQ = 0;
-constexpr int kPfOffP = kPfQBytes;
+constexpr int kPfOffP = 0;
 constexpr int kPfOffRing = kPfOffP + 2 * kPfPBytes;
 constexpr int kPfOffBars = kPfOffRing + kPfRing * kPfPiece;
 constexpr int kPfSmem = kPfOffBars + (int)sizeof(PfBars) + 1024;  // + slack for the 1024-byte alignment
@@ -97,8 +99,7 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& a, int it) {
   return x;
 }
 
-// Loader: per item the Q tile (once every QK of the previous item has
-// completed), then the pieces with K two tiles ahead of V: K(0), K(1), then
+// Loader: per item the pieces with K two tiles ahead of V: K(0), K(1), then
 // K(j), V(j-2) for j = 2 .. nt-1, then the last two V.  K(j) = 4 pieces (d
 // atoms), V(j) = 4 pieces (32 keys each).  With K ahead, the ring never
 // holds back QK(j+2) behind PV(j), which waits for the softmax.  Keys past
@@ -111,9 +112,6 @@ __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
   for (int it = blockIdx.x; it < a.total_items; it += gridDim.x) {
     const PfItem x = pf_item(a, it);
     if (x.nt == 0) continue;
-    if (!mbar_wait(&M.q_empty, (n & 1) ^ 1, ctl)) break;
-    tma_load_5d(smem_u32(sm + kPfOffQ), &a.q_map, 0, x.qt * kPfRows, 0, x.h, x.b, &M.q_full);
-    mbar_arrive_expect_tx(&M.q_full, kPfQBytes);
     ++n;
     const int g = x.h / a.G;
     bool ok = true;
@@ -143,7 +141,6 @@ __device__ void pf_loader(const PrefillArgs& a, PfBars& M, uint8_t* sm) {
   if (ctl->abort) {
     // let this thread's copies in flight land before the CTA exits
     if (f > 0) mbar_drain(&M.full[(f - 1) % kPfRing], ((f - 1) / kPfRing) & 1, ctl);
-    if (n > 0) mbar_drain(&M.q_full, (n - 1) & 1, ctl);
   }
 }
 
@@ -158,15 +155,14 @@ __device__ __forceinline__ uint32_t pf_fill_v(uint32_t f0, int j, int nt) {
 }
 
 // QK issuer (one thread): S(j) = Q K(j)^T over 4 pieces (d atoms) of 4
-// steps each, into S buffer j & 1 once the softmax has read S(j-2) out of
-// it.  Each ring piece is released by a commit after the products that read
-// it.  The two issuers run on separate threads so that
+// steps each, once the softmax has written the item's Q rows into TMEM and
+// has read S(j-1) out of the S columns.  Each ring piece is released by a
+// commit after the products that read it.  The two issuers run on separate threads so that
 // their instruction streams overlap (one thread issues an MMA every 100 or
 // so cycles, slower than the tensor core runs these shapes).
 __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t tb) {
   constexpr uint32_t id_qk = idesc_f16(128, 128, 0, 0, 0);
   WaitCtl* ctl = &M.ctl;
-  const uint64_t q_desc = sdesc_sw128(smem_u32(sm + kPfOffQ), 16, 1024);
   const uint32_t ring0 = smem_u32(sm + kPfOffRing);
   uint32_t f0 = 0, jg = 0;  // first fill of the item, tiles of earlier items
   int n = 0;                // items started
@@ -177,8 +173,8 @@ __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
     tc_fence_after();
     for (int j = 0; j < x.nt; ++j) {
       const uint32_t jj = jg + j;
-      if (jj >= 2 && !mbar_wait(&M.s_free[jj & 1], ((jj - 2) >> 1) & 1, ctl)) return;
-      const uint32_t s_col = tb + kPfColS + (jj & 1) * 128;
+      if (jj >= 1 && !mbar_wait(&M.s_free, (jj - 1) & 1, ctl)) return;
+      const uint32_t s_col = tb + kPfColS;
       const uint32_t fk = pf_fill_k(f0, j);
       for (int at = 0; at < 4; ++at) {
         const uint32_t idx = fk + at, slot = idx % kPfRing, use = idx / kPfRing;
@@ -187,12 +183,11 @@ __device__ void pf_mma_qk(const PrefillArgs& a, PfBars& M, uint8_t* sm, uint32_t
         const uint64_t k_desc = sdesc_sw128(ring0 + slot * kPfPiece, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(s_col, sdesc_add(q_desc, at * 16384 + kk * 32), sdesc_add(k_desc, kk * 32), id_qk,
+          mma_ts(s_col, tb + kPfColQ + (uint32_t)(4 * at + kk) * 8, sdesc_add(k_desc, kk * 32), id_qk,
                  (at | kk) != 0 ? 1u : 0u);
         mma_commit(&M.empty[slot]);
       }
-      mma_commit(&M.s_full[jj & 1]);
-      if (j == x.nt - 1) mma_commit(&M.q_empty);
+      mma_commit(&M.s_full);
     }
     f0 += 8u * x.nt;
     jg += x.nt;
@@ -271,19 +266,41 @@ __device__ void pf_softmax(const PrefillArgs& a, PfBars& M, int warp, int lane, 
     const long long lim = (long long)a.kv_len - a.q_len + (long long)x.qt * kPfRows + r + 1;
     const long long vis_end = lim < x.k1 ? lim : x.k1;
     float m_ref = kPfNoMax, l = 0.0f;
+    // the item's Q row into TMEM columns 0-127 (query 128 qt + r of head h,
+    // zeros past q_len); every QK of the previous item has completed (its
+    // last S was read before this point)
+    {
+      const int qi = x.qt * kPfRows + r;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.q) +
+                                                        (((size_t)x.b * a.q_len + qi) * a.Hq + x.h) * 256);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint4 v4 = qi < a.q_len ? __ldg(src + 4 * c + e) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * e] = v4.x, w[4 * e + 1] = v4.y, w[4 * e + 2] = v4.z, w[4 * e + 3] = v4.w;
+        }
+        PA_TMEM_ST_X16(lane_base + kPfColQ + 16 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&M.q_full);
+    }
     for (int j = 0; j < x.nt; ++j, ++jg) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&M.s_full[jg & 1], (jg >> 1) & 1, ctl))) return;
+      if (!__all_sync(0xffffffffu, mbar_wait(&M.s_full, jg & 1, ctl))) return;
       tc_fence_after();
-      const uint32_t s_addr = lane_base + kPfColS + (jg & 1) * 128;
+      const uint32_t s_addr = lane_base + kPfColS;
       uint32_t u[128];
 #pragma unroll
       for (int c = 0; c < 8; ++c) PA_TMEM_LD_X16(s_addr + 16 * c, (u + 16 * c));
       tmem_wait_ld();
       reg_fence(u);
-      // S(j) is in registers: QK(j+2) may overwrite its buffer
+      // S(j) is in registers: QK(j+1) may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&M.s_free[jg & 1]);
+      if (lane == 0) mbar_arrive(&M.s_free);
       const long long t0 = (long long)x.k0 + (long long)j * kPfKeys;
       const long long nv = vis_end - t0;
       const int nvis = nv <= 0 ? 0 : (nv >= kPfKeys ? kPfKeys : (int)nv);
@@ -387,11 +404,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       mbar_init(&M.full[s], 1);
       mbar_init(&M.empty[s], 1);
     }
-    mbar_init(&M.q_full, 1);
-    mbar_init(&M.q_empty, 1);
+    mbar_init(&M.q_full, 4);  // one arrival per softmax warp
+    mbar_init(&M.s_full, 1);
+    mbar_init(&M.s_free, 4);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&M.s_full[s], 1);
-      mbar_init(&M.s_free[s], 4);  // one arrival per softmax warp
       mbar_init(&M.p_full[s], 4);  // one arrival per softmax warp
       mbar_init(&M.pv_done[s], 1);
     }
