@@ -20,6 +20,11 @@ Printed JSON (one line, rank 0):
   cpu_baseline  the FP64 oracle on a bounded sample, on this host's cores
 
 --impl reference times the oracle itself as the comparison arm.
+
+--workload prefill_q8192_kv262144 (or another name of workloads.PREFILL_SPECS)
+times the causal prefill instead: one step = one pa_prefill_f16 call; value in
+logical causal TFLOP/s; the tensor roofline of its attention kernel against the
+measured sustained BF16 GEMM rate.
 Multi-GPU (torchrun): independent replicas, one per rank (no data-path
 collective); the barrier and the max over ranks use torch.distributed.
 """
