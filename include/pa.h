@@ -145,9 +145,11 @@ int pa_split_plan(int32_t ctx_len, int32_t num_kv_heads, int32_t* num_splits, in
 /* ---- FP16 Q x E4M3 K/V, head_dim 256 ---------------------------------------
  *
  * Workspace bytes a pa_decode_fp8 call with this geometry needs (0 when the
- * geometry is invalid).  The workspace holds the status word and the
- * request-major FP32 split partials; its content between calls is only the
- * status word. */
+ * geometry is invalid).  The workspace holds the status word, per-call
+ * counters and flags, and the request-major FP32 split partials.  It must
+ * be zero-filled before its first use (for example one cudaMemset after
+ * allocation); every call leaves the counters and flags at zero again, so
+ * between calls only the status word carries information. */
 size_t pa_decode_fp8_workspace_bytes(const pa_params* p);
 
 /* q           FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned.
@@ -159,8 +161,9 @@ size_t pa_decode_fp8_workspace_bytes(const pa_params* p);
  * v_scale     one FP32 in device memory: a V element is E4M3(byte) * *v_scale.
  *             (Device pointers, so a captured graph can be replayed with new scales.)
  * out         FP16 [batch][q_len][num_q_heads][256], contiguous, 16-byte aligned; fully written.
- * workspace   device buffer of at least pa_decode_fp8_workspace_bytes(p) bytes, 256-byte aligned;
- *             two calls in flight at the same time must use different workspaces.
+ * workspace   device buffer of at least pa_decode_fp8_workspace_bytes(p) bytes, 256-byte aligned,
+ *             zero-filled before its first use; two calls in flight at the same time must use
+ *             different workspaces.
  * stream      cudaStream_t (NULL = legacy default stream).
  * QK^T and PV run on the tensor cores with FP16 inputs and FP32 accumulation
  * ("SM70 attention and quantized projection coverage across TP sizes", section
@@ -348,8 +351,8 @@ int pa_prefill_f16(const pa_prefill_params* p, const void* q, const void* k, con
  * threads; `device` and `stream` are only compared, never used.
  *
  * pa_bank_alloc_fn  returns `bytes` bytes of ZERO-FILLED device memory on
- *                   `device`, 256-byte aligned (the workspace's status word
- *                   must start at zero), or NULL.  Called with the bank's
+ *                   `device`, 256-byte aligned (a decode workspace must be
+ *                   zero before its first use), or NULL.  Called with the bank's
  *                   lock held: it must not call back into the bank.
  * pa_bank_free_fn   returns a panel to the caller (NULL: the caller keeps
  *                   ownership of every panel). */

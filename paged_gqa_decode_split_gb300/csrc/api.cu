@@ -277,8 +277,9 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* bad = reinterpret_cast<uint32_t*>(ws + kWsBadOff);
-  // per-request flags, split arrival counters and the merge-task counter start at zero
-  if (cudaMemsetAsync(bad, 0, kWsClearBytes, stream) != cudaSuccess) return PA_ERR_CUDA;
+  // the per-request flags, split arrival counters and task counters are zero
+  // between calls (the workspace is zero at first use; the last CTA of every
+  // call resets them), so a call is one launch
   if (clear_status && cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return PA_ERR_CUDA;
 
   SplitArgs a;
@@ -298,6 +299,7 @@ int decode_common(KvFormat fmt, const pa_params* p, const void* q, const void* k
   a.bad = bad;
   a.arrive = reinterpret_cast<uint32_t*>(ws + kWsArriveOff);
   a.queue = reinterpret_cast<uint32_t*>(ws + kWsQueueOff);
+  a.done = reinterpret_cast<uint32_t*>(ws + kWsDoneOff);
   a.k_ps = p->k_page_stride, a.k_ts = p->k_token_stride, a.k_hs = p->k_head_stride;
   a.v_ps = p->v_page_stride, a.v_ts = p->v_token_stride, a.v_hs = p->v_head_stride;
   a.B = p->batch, a.Hkv = p->num_kv_heads, a.Hq = p->num_q_heads, a.G = p->num_q_heads / p->num_kv_heads;

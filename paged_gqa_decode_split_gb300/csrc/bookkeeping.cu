@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(64) worklist_kernel(const int32_t* ctx_lens, i
                                                       int32_t* items, int32_t max_items, int32_t* count,
                                                       uint32_t* status) {
   __shared__ Sched S;
-  sched_build(S, ctx_lens, B, Hkv, max_ctx, status, nullptr);
+  sched_build(S, threadIdx.x < B ? ctx_lens[threadIdx.x] : 0, B, Hkv, max_ctx, status, nullptr);
   if (threadIdx.x == 0) *count = S.total;
   for (int it = threadIdx.x; it < S.total && it < max_items; it += blockDim.x) {
     const Item x = sched_item(S, B, it);

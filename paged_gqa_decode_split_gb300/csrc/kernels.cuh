@@ -56,6 +56,7 @@ struct SplitArgs {
   uint32_t* bad;
   uint32_t* arrive;            // per request: softmax-group arrivals of its finished split items
   uint32_t* queue;             // next merge task
+  uint32_t* done;              // CTAs that finished the call (the last one resets the per-call words)
   long long k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
   int B, Hkv, Hq, G, q_len, R, page_size, mpr, num_pages, max_ctx, s_max;
   long long wait_limit;  // pipeline wait bound in cycles (0: default)

@@ -55,9 +55,10 @@ __host__ __device__ inline int max_splits_for(int max_ctx_len) {
 
 // ------------------------------------------------------------ workspace --
 // [0, 4)          status word (PA_FLAG_* bits, sticky)
-// [512, 768)      per-request "bad input" flags            } cleared by the host
-// [768, 1024)     per-request split arrival counters        } API before every
-// [1024, 1028)    next combine task (the merge phase's queue) } call
+// [512, 768)      per-request "bad input" flags             } zero between calls:
+// [768, 1024)     per-request split arrival counters        } the last CTA of a
+// [1024, 1028)    next merge task (the merge phase's queue) } call resets them
+// [1028, 1032)    CTAs that finished the call               } (zero at first use)
 // [1280, ...)     panel_ml: float2 (m, l) [B][Hkv][S_max][R]
 // [...]           panel_o : float      [B][Hkv][S_max][R][D]   (unnormalised partial O)
 struct WsLayout {
@@ -74,7 +75,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int Hkv, int s_max, int R, 
 constexpr size_t kWsBadOff = 512;      // uint32 [kMaxBatch]
 constexpr size_t kWsArriveOff = 768;   // uint32 [kMaxBatch]
 constexpr size_t kWsQueueOff = 1024;   // uint32
-constexpr size_t kWsClearBytes = 768;  // bytes cleared from kWsBadOff on: flags, counters and queue
+constexpr size_t kWsDoneOff = 1028;    // uint32
 
 // ------------------------------------------------------------- schedule --
 // Every CTA derives the same ordered item list from ctx_lens: requests sorted
@@ -96,11 +97,13 @@ struct Item {
 
 // Called by every thread of the CTA (uses __syncthreads).  Invalid lengths
 // (< 0 or > max_ctx) count as 0 and raise PA_FLAG_BAD_LENGTH once (CTA 0).
-__device__ inline void sched_build(Sched& S, const int32_t* ctx_lens, int B, int Hkv, int max_ctx,
-                                   uint32_t* status, uint32_t* bad) {
+// len_t: ctx_lens[threadIdx.x] for threads below B (loaded by the caller,
+// which may issue the load early), unused otherwise.
+__device__ inline void sched_build(Sched& S, int len_t, int B, int Hkv, int max_ctx, uint32_t* status,
+                                   uint32_t* bad) {
   int t = threadIdx.x;
   if (t < B) {
-    int L = ctx_lens[t];
+    int L = len_t;
     if (L < 0 || L > max_ctx) {
       if (blockIdx.x == 0) {
         if (status) atomicOr(status, 0x2u);

@@ -162,6 +162,12 @@ __device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
 }
 
 // Prefetch of the cache line holding `p` into L2.
+// Atomic add at GPU scope with acquire-release ordering; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // ----------------------------------------------------------------- cp.async --

@@ -1207,6 +1207,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
   uint8_t* sm = smem_base();
   Misc& M = *reinterpret_cast<Misc*>(sm + L::kOffMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the request lengths and the block table are the first things the
+  // schedule and the loaders read: their loads start before the prologue
+  const int len_t = tid < a.B ? ld_page_id(a.ctx_lens + tid) : 0;
+  if (warp == 2) {
+    const size_t bt_bytes = (size_t)a.B * a.mpr * 4;
+    const size_t n = bt_bytes < 65536 ? bt_bytes : 65536;
+    for (size_t off = (size_t)lane * 128; off < n; off += 32 * 128)
+      prefetch_l2(reinterpret_cast<const char*>(a.block_table) + off);
+  }
 
   if (tid == 0) {
     mbar_init(&M.kst_full, TMA != 0 ? 1 : 32);
@@ -1240,7 +1249,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     *reinterpret_cast<uint4*>(sm + L::kOffQ + o) = make_uint4(0, 0, 0, 0);
   for (int o = tid * 16; o < kPBufs * 16384; o += kThreads * 16)
     *reinterpret_cast<uint4*>(sm + L::kOffP + o) = make_uint4(0, 0, 0, 0);
-  sched_build(M.sched, a.ctx_lens, a.B, a.Hkv, a.max_ctx, a.status, a.bad);  // contains __syncthreads
+  sched_build(M.sched, len_t, a.B, a.Hkv, a.max_ctx, a.status, a.bad);  // contains __syncthreads
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -1299,10 +1308,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const __grid_constan
     tmem_dealloc(tb, 512);
   }
   if (M.ctl.abort) {
-    if (tid == 0) atomicOr(a.status, 0x4u);
-    return;  // the call's output is invalid; other CTAs' merge waits run out
+    if (tid == 0) atomicOr(a.status, 0x4u);  // the call's output is invalid; other CTAs' merge waits run out
+  } else {
+    merge_phase<Fmt>(a, M, tid);
   }
-  merge_phase<Fmt>(a, M, tid);
+  // the last CTA to finish returns the per-call words of the workspace to
+  // zero for the next call (every CTA has finished reading them by then)
+  __syncthreads();
+  if (tid == 0 && atom_add_acq_rel_u32(a.done, 1u) == gridDim.x - 1) {
+    for (int b = 0; b < a.B; ++b) a.arrive[b] = 0u, a.bad[b] = 0u;
+    *a.queue = 0u;
+    *a.done = 0u;
+  }
 }
 
 template <class Fmt, int NM, int TMA>

@@ -499,3 +499,23 @@ def test_wait_bound_runs_out_cleanly():
     assert dec.status() == 0
     check_full(w, dec.out)
     assert B.pa_debug_stall_next(0) == B.PA_ERR_SHAPE
+
+
+def test_per_call_words_return_to_zero():
+    """A decode call leaves its per-request flags, arrival counters and task
+    counters at zero (the last CTA resets them), also after a call that saw
+    a bad length, so the next call on the same workspace needs no clearing."""
+    w = _small("fp8", [3000, 700, 37], seed=23)
+    dec = D.Decoder(w)
+    good = w.ctx_lens.clone()
+    for lens in (good, torch.tensor([3000, 10**9, 37], dtype=torch.int32, device="cuda"), good):
+        w.ctx_lens.copy_(lens)
+        dec.run()
+        torch.cuda.synchronize()
+        words = dec.workspace[512:1032].view(torch.int32)
+        assert torch.count_nonzero(words) == 0
+    B.check(B.pa_clear_status(dec.workspace), "clear")
+    dec.run()
+    torch.cuda.synchronize()
+    assert dec.status() == 0
+    check_full(w, dec.out)
