@@ -196,9 +196,9 @@ int pa_decode_fp8(const pa_params* p, const void* q, const void* k_pages, const 
  * device at set-up, before any stream capture and before the latency-critical
  * phase; from the second call on nothing is allocated or loaded.  Every call
  * on a device shares the one array, which keeps the last call's contents;
- * each call clears the parts that must start at zero (status word,
- * per-request flags), so a bad input flagged by one call does not carry into
- * the next.
+ * each call clears the status word first, and its kernel returns the
+ * per-request flags and counters to zero as it finishes (the array starts at
+ * zero), so a bad input flagged by one call does not carry into the next.
  * Calls that overlap on the GPU (different streams, or several host threads)
  * race on the array and give undefined results: serialise them.  The status
  * word is cleared at the start of every call and cannot be read back.
