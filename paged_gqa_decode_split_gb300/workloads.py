@@ -288,9 +288,12 @@ PREFILL_SPECS = {
     # the TP2 / TP1 local geometries, B2 (the bitwise per-head check's shapes)
     "prefill_q8192_kv262144_hkv2_b2": PrefillSpec("prefill_q8192_kv262144_hkv2_b2", 2, 8192, 262144, 12, 2),
 }
+# the TP1 local geometry (Hkv 4, Hq 24) of the same page
+PREFILL_SPECS["prefill_q8192_kv262144_hkv4"] = PrefillSpec("prefill_q8192_kv262144_hkv4", 1, 8192, 262144, 24, 4)
 # a smaller case of the same kernel for profiler captures (K and V still exceed L2)
 PREFILL_SPECS["prefill_q2048_kv131072"] = PrefillSpec("prefill_q2048_kv131072", 1, 2048, 131072, 6, 1)
-PREFILL_SEED = {"prefill_q8192_kv262144": 2001, "prefill_q8192_kv262144_hkv2_b2": 2002, "prefill_q2048_kv131072": 2003}
+PREFILL_SEED = {"prefill_q8192_kv262144": 2001, "prefill_q8192_kv262144_hkv2_b2": 2002, "prefill_q2048_kv131072": 2003,
+                "prefill_q8192_kv262144_hkv4": 2004}
 
 
 def generate_prefill(spec: PrefillSpec, seed: int, device: str | torch.device = "cpu") -> PrefillWorkload:
