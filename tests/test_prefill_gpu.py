@@ -152,3 +152,39 @@ def test_prefill_large_magnitude_inputs():
     assert torch.isfinite(pf.out).all()
     ref, rlse = run_prefill_oracle(w)
     _compare(to_f64(pf.out), ref, _visible(spec), pf.lse, rlse, rel_elem=DOMINANT_REL)
+
+
+def test_prefill_graph_replay_with_changed_inputs_bitwise():
+    """The section "Graph replay and long-prefill follow-up": a captured prefill
+    replayed after another kv_len was captured and after every input changed
+    gives the bits of an ordinary call on the new inputs (parameters travel by
+    value; no host memory is captured)."""
+    spec_a = wl.PrefillSpec("graph_a", 1, 200, 5000, 6, 1)
+    spec_b = wl.PrefillSpec("graph_b", 1, 130, 2100, 6, 1)
+    wa = wl.generate_prefill(spec_a, 90, device="cuda")
+    wb = wl.generate_prefill(spec_b, 91, device="cuda")
+    pa, pb = Prefill(wa), Prefill(wb)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graphs = []
+    for pf in (pa, pb):
+        pf(stream.cuda_stream)  # warm-up outside the capture (module loading, attributes)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            B.check(pf(torch.cuda.current_stream().cuda_stream), "captured prefill")
+        graphs.append(g)
+    # new contents for every input of the first graph, then replay it
+    fresh = wl.generate_prefill(spec_a, 92, device="cuda")
+    wa.q.copy_(fresh.q)
+    wa.k_buf.copy_(fresh.k_buf)
+    wa.v_buf.copy_(fresh.v_buf)
+    graphs[1].replay()
+    graphs[0].replay()
+    torch.cuda.synchronize()
+    replayed = pa.out.clone()
+    eager = Prefill(wa)
+    eager.run()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed.view(torch.int16), eager.out.view(torch.int16))
+    assert pa.status() == 0
