@@ -394,10 +394,47 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
 #pragma unroll
           for (int k = 0; k < 4; ++k) pq[k] = pq_tile[k];
         }
+        // Windows and two-fill tiles: the fill's first piece is located before
+        // the stage is free.  A whole tile inside one page is one box, and its
+        // byte count is armed on the full barrier as soon as the previous fill
+        // has landed (the phase then waits for the bytes alone), so that once
+        // the decode warps release the stage only the copy itself is left to
+        // issue.  Single-fill 16-byte aligned tiles measured slower with this
+        // order and take the general path below.
+        constexpr bool kPreArm = Win || Fmt::kFills == 2;
+        bool whole = false;
+        int slot0 = 0, pg0 = -1;
+        if constexpr (kPreArm) {
+          const int q0 = kb / ps;
+          slot0 = kb - q0 * ps;
+          for (int adv = 0; adv < kTileKeys / 16 && q_cur < q0; ++adv) {
+            pq[0] = pq[1], pq[1] = pq[2], pq[2] = pq[3];
+            ++q_cur;
+            pq[3] = q_cur + 3 <= q_last ? ld_page_id(bt + q_cur + 3) : -1;
+          }
+          pg0 = pq[0];
+          whole = rows == kTileKeys && slot0 + kTileKeys <= ps && (unsigned)pg0 < (unsigned)a.num_pages;
+          if (whole) {
+            if (f > 0 && !mbar_wait(full, (f - 1) & 1, abort)) {
+              mbar_drain(full, (f - 1) & 1, abort);
+              return;
+            }
+            mbar_arrive_expect_tx(full, Win ? kTileKeys * kWinRowBytes : kTileKeys * 256);
+          }
+        }
         if (!mbar_wait(empty, (f & 1) ^ 1, abort)) {
           // fill f - 1 may still be landing: let it finish before the CTA exits
           if (f > 0) mbar_drain(full, (f - 1) & 1, abort);
           return;
+        }
+        if (whole) {
+          if constexpr (Win) {
+            // window element 128h is the byte 8 before row byte 256h
+            tma_load_4d_hint(dst_base, maps, 128 * h, x.g, slot0, pg0, full, once);
+          } else {
+            tma_load_5d_hint(dst_base, tile_map, 0, x.g, slot0, 2 * h, pg0, full, once);
+          }
+          continue;
         }
         uint32_t bytes = 0;
         bool bad = false;
@@ -699,6 +736,9 @@ __device__ __forceinline__ void role_kdecode(const SplitArgs& a, Misc& M, int i,
         // tensor core
         uint4 raw[16];
         load_row<Win>(stage, 32 * i + lane, x.t0 + jl * kTileKeys + 32 * i + lane < x.t1, raw);
+        // the row reads (generic proxy) are ordered before the next fill,
+        // which the TMA writes through the async proxy once the stage is free
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.kst_empty);
         // K'[j&1] is free once QK(j-2) is done (its completion is s_full's phase)
@@ -760,6 +800,7 @@ __device__ __forceinline__ void role_vdecode(const SplitArgs& a, Misc& M, int i,
         // row into registers, stage back to the loader, then wait for the slot
         uint4 raw[16];
         load_row<Win>(stage, key, x.t0 + jl * kTileKeys + key < x.t1, raw);
+        fence_proxy_async_smem();  // the row reads before the next fill's TMA writes
         __syncwarp();
         if (lane == 0) mbar_arrive(&M.vst_empty);
         if (h == 0 && c >= (uint32_t)L::kVSlots) {
