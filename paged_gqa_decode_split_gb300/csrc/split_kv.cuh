@@ -67,6 +67,9 @@ struct Fp8Fmt {
   static constexpr int kElemBytes = 1;
   static constexpr int kFills = 1;                 // staging fills per tile
   static constexpr int kQBf16 = 0;                 // Q (and K') type of the QK product
+  // the TMA loader arms a whole in-page fill before its stage is released
+  // (windows always do): measured per format, faster for FP16 only
+  static constexpr bool kPreArm = false;
   static __device__ __forceinline__ float score_scale(const float* k_scale) {
     // S' = q . k_code;  s * log2(e) = S' * k_scale / sqrt(256) * log2(e)
     return __ldg(k_scale) * (1.0f / 16.0f) * 1.4426950408889634f;
@@ -96,6 +99,7 @@ struct Bf16Fmt {
   static constexpr int kElemBytes = 2;
   static constexpr int kFills = 1;
   static constexpr int kQBf16 = 1;
+  static constexpr bool kPreArm = false;
   static __device__ __forceinline__ float score_scale(const float*) {
     return 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
   }
@@ -124,6 +128,7 @@ struct F16Fmt {
   static constexpr int kElemBytes = 2;
   static constexpr int kFills = 2;
   static constexpr int kQBf16 = 0;
+  static constexpr bool kPreArm = true;
   static __device__ __forceinline__ float score_scale(const float*) {
     return 1.4426950408889634f * (1.0f / 16.0f);  // log2(e) / sqrt(256)
   }
@@ -394,14 +399,14 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
 #pragma unroll
           for (int k = 0; k < 4; ++k) pq[k] = pq_tile[k];
         }
-        // Windows and two-fill tiles: the fill's first piece is located before
-        // the stage is free.  A whole tile inside one page is one box, and its
-        // byte count is armed on the full barrier as soon as the previous fill
-        // has landed (the phase then waits for the bytes alone), so that once
-        // the decode warps release the stage only the copy itself is left to
-        // issue.  Single-fill 16-byte aligned tiles measured slower with this
-        // order and take the general path below.
-        constexpr bool kPreArm = Win || Fmt::kFills == 2;
+        // Windows and FP16 tiles: the fill's first piece is located before the
+        // stage is free.  A whole tile inside one page is one box, and its byte
+        // count is armed on the full barrier as soon as the previous fill has
+        // landed (the phase then waits for the bytes alone), so that once the
+        // decode warps release the stage only the copy itself is left to issue.
+        // The other 16-byte aligned formats measured slower with this order and
+        // take the general path below.
+        constexpr bool kPreArm = Win || Fmt::kPreArm;
         bool whole = false;
         int slot0 = 0, pg0 = -1;
         if constexpr (kPreArm) {
