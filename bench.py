@@ -325,6 +325,22 @@ def run_gpu(args, dist, rank, world, local):
         if d.status() != 0:
             raise RuntimeError(f"status flags {d.status():#x} after warm-up")
 
+    # the timed steps replay one CUDA graph holding a pass over the working
+    # sets (calls in rotation), as a decode step is deployed; a remainder of
+    # steps runs as direct calls, so exactly args.steps calls are timed
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(nsets):
+            B.check(decs[i](side), "graph warm-up call")
+    stream.wait_stream(side)
+    pass_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pass_graph):
+        for i in range(nsets):
+            B.check(decs[i](torch.cuda.current_stream(dev)), "captured call")
+    pass_graph.replay()
+    torch.cuda.synchronize(dev)
+
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", "") or "")
     sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local)))
@@ -337,14 +353,26 @@ def run_gpu(args, dist, rank, world, local):
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        B.check(decs[i % nsets](stream), "timed call")
+    for _ in range(args.steps // nsets):
+        pass_graph.replay()
+    for i in range(args.steps % nsets):
+        B.check(decs[i](stream), "timed call")
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
     timed_bytes = sum(uniq[i % nsets] for i in range(args.steps))
+    del pass_graph
+    # the same calls launched one by one from the host (no graph), for reference
+    n_direct = min(args.steps, 512)
+    ed0, ed1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ed0.record(stream)
+    for i in range(n_direct):
+        B.check(decs[i % nsets](stream), "direct call")
+    ed1.record(stream)
+    torch.cuda.synchronize(dev)
+    direct_us = ed0.elapsed_time(ed1) * 1e3 / n_direct
     # roofline burst: the same calls back to back, CUDA events around every
     # kernel launch; a whole number of passes over the sets
     n_roof = max(16, -(-args.roofline_launches // nsets) * nsets)
@@ -353,9 +381,36 @@ def run_gpu(args, dist, rank, world, local):
         B.check(decs[i % nsets](stream), "roofline call")
     B.pa_timing_enable(False)
     torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
     st0, split_ms, split_n = B.pa_timing_collect(0)
     roof_bytes = sum(uniq[i % nsets] for i in range(n_roof))
+    # the operator measurement protocol of "DFlash2 concurrent long-context
+    # attention": one CUDA graph of 16 calls (the working sets in rotation),
+    # replayed 8 times per sample; per call, the median of 5 samples
+    g_calls, g_reps, g_samples = 16, 8, 5
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(g_calls):
+            B.check(decs[i % nsets](side), "graph warm-up call")
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(g_calls):
+            B.check(decs[i % nsets](torch.cuda.current_stream(dev)), "captured call")
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    g_us = []
+    for _ in range(g_samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(g_reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        g_us.append(e0.elapsed_time(e1) * 1e3 / (g_calls * g_reps))
+    g_bytes = sum(uniq[i % nsets] for i in range(g_calls)) / g_calls
+    del graph
+    clocks = sampler.stop()
     for d in decs:
         if d.status() != 0:
             raise RuntimeError(f"status flags {d.status():#x} after the timed region")
@@ -406,7 +461,11 @@ def run_gpu(args, dist, rank, world, local):
     total_bytes = timed_bytes * world
     value = total_bytes / (ms / 1e3) / 1e9
     split_avg_s = split_ms / max(split_n, 1) / 1e3
-    achieved = roof_bytes / max(split_n, 1) / split_avg_s / 1e9
+    # every launch in the timed region is this kernel (one per call), so its
+    # average launch duration is the region's time per call (it includes the
+    # gaps between consecutive graph nodes: a slight underestimate of the rate)
+    kernel_avg_s = ms / 1e3 / args.steps
+    achieved = timed_bytes / args.steps / kernel_avg_s / 1e9
     traffic = _traffic(name)
     rotated = sum(uniq)
     l2_note = (f"no flush: every step's KV ({min(uniq) / 1e6:.0f} MB or more) exceeds the 129 MB L2"
@@ -432,12 +491,27 @@ def run_gpu(args, dist, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": f"split-KV kernel with its merge phase (the one kernel of {entry_point(spec)})",
-                     "kernel_avg_us": split_avg_s * 1e6,
-                     "timed_launches": split_n,
-                     "algorithmic_bytes_per_launch": roof_bytes / max(split_n, 1),
-                     "timing": f"CUDA events around each of {split_n} kernel launches of a burst of "
-                               f"{n_roof} calls after the timed region"},
+                     "kernel_avg_us": kernel_avg_s * 1e6,
+                     "timed_launches": args.steps,
+                     "algorithmic_bytes_per_launch": timed_bytes / args.steps,
+                     "timing": "CUDA events on the launching stream around the timed region, which holds "
+                               "only this kernel's launches (one per call)",
+                     "per_launch_events_us": split_avg_s * 1e6,
+                     "per_launch_events": f"CUDA events around each of {split_n} kernel launches of a burst of "
+                                          f"{n_roof} calls after the timed region (the events hold back "
+                                          f"back-to-back launches)",
+                     "per_launch_events_bytes_per_launch": roof_bytes / max(split_n, 1)},
         "gpu_launches": args.steps,
+        "timing": f"{args.steps // nsets} replays of a CUDA graph of {nsets} calls (one per working set)"
+                  + (f" + {args.steps % nsets} direct calls" if args.steps % nsets else "")
+                  + ", CUDA events on the launching stream",
+        "direct": {"us_per_call": direct_us, "calls": n_direct,
+                   "note": "the same calls launched one by one from the host, after the timed region"},
+        "graph": {"us_per_call": statistics.median(g_us), "GBps": g_bytes / statistics.median(g_us) / 1e3,
+                  "pct_of_hbm_peak": 100.0 * g_bytes / statistics.median(g_us) / 1e3 / peak,
+                  "samples_us": g_us, "calls_per_graph": g_calls, "replays_per_sample": g_reps,
+                  "note": "one CUDA graph of 16 calls (working sets in rotation), 8 replays per sample, "
+                          "median of 5 samples per call; this GPU's calls"},
         "clocks": clocks,
         "e2e": {"value": unique * e_steps * world / e2e_s / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
