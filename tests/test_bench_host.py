@@ -62,6 +62,20 @@ def test_reference_arm_single_process():
     assert ln["e2e"]["h2d_bytes_per_step"] == 0 and ln["steps"] == 3 and ln["warmup"] == 3
 
 
+def test_reference_arm_prefill_single_process():
+    """The prefill workload's reference arm: the FP64 oracle on a bounded
+    sample of output rows, reported in the prefill metric's unit."""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "prefill_q8192_kv262144",
+                        "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    ln = lines[0]
+    assert ln["impl"] == "reference" and ln["value"] > 0 and ln["unit"] == "TFLOP/s"
+    assert ln["cpu_baseline"]["kind"] == "oracle" and ln["cpu_baseline"]["cores"] >= 1
+    assert ln["e2e"] == {"value": ln["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
 def test_reference_arm_two_ranks_rank0_only():
     port = _free_port()
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
