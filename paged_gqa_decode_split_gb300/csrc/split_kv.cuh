@@ -375,7 +375,7 @@ __device__ __forceinline__ void role_loader_tma(const SplitArgs& a, Misc& M, boo
   const int ps = a.page_size;
   const uint32_t dst_base = smem_u32(stage);
   // K and V are read once per call: evict them from L2 first, so that the
-  // split partials the combine kernel reads next stay resident
+  // split partials the merge phase reads at the end of the grid stay resident
   const uint64_t once = l2_policy_evict_first();
   uint32_t f = 0;  // fills issued
   for (int it = blockIdx.x; it < M.sched.total; it += gridDim.x) {
@@ -918,7 +918,7 @@ __device__ __forceinline__ void role_softmax(const SplitArgs& a, Misc& M, int gr
   const int bar_id = kSoftmaxBar + grp;
   const float c_log2 = Fmt::score_scale(a.k_scale);
   const uint32_t lane_base = tb + ((uint32_t)(32 * i) << 16);
-  // the split partials are read back by the combine kernel right after this
+  // the split partials are read back by the merge phase at the end of this
   // grid: keep their L2 lines
   const uint64_t keep = l2_policy_evict_last();
   const int rbase = BF::base(lane);  // rows row0+rbase .. +CNT-1 of every butterfly result
